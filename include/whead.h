@@ -1,0 +1,137 @@
+/*
+ * whead.h — C ABI of the walk-resident serial draft head for GB300 (sm_103a).
+ *
+ * The operation ("Weights That Stay: On-Chip Megakernels for Serial Heads in Speculative Decoding",
+ * abstract; Figs. 1, 2, 7, 8): a parallel block drafter has produced base logits for gamma positions;
+ * a light serial head then walks those positions one by one. Step t projects a small state u_t (rank r)
+ * through one immutable V x r matrix W, adds the base logits, picks one token over all V rows (greedy,
+ * or Gumbel-max sampling at temperature T), and advances the state from the picked token:
+ *   Markov head:    u_{t+1} = E[x_t]
+ *   recurrent head: h_{t+1} = tanh(A h_t + E[x_t] + c), u_t = h_t
+ * The state is rounded to bf16 before the projection; the projection accumulates in fp32; z = p + base
+ * is formed in fp32 and rounded once when it is emitted; ties go to the smallest row index. The noise
+ * for T > 0 is Philox4x32-10 keyed on (seed lo, seed hi) with counter (v/4, t0 + t, b, 0), word v%4,
+ * U = ((w >> 9) + 0.5) * 2^-23, g = -log(-log U), key = z / T + g.
+ *
+ * Execution: one persistent cooperative kernel per walk. Each CTA keeps its shard of W on chip (shared
+ * memory, tensor memory and registers) for the whole walk and exchanges only packed {key, row} words and
+ * the compact state between steps (Fig. 1; Fig. 8).
+ *
+ * Conventions for every call below:
+ *  - Pointers named W, E, A, c, base, u0/s0 and out_* are DEVICE pointers unless the name says host.
+ *  - W, E (and A, c) are borrowed for the lifetime of the handle and must not change (W is immutable
+ *    for the whole walk). Call inputs and outputs are borrowed for the call; the caller allocates them.
+ *  - The handle owns only its scratch (exchange slots, counters, status word, staging buffers).
+ *  - Calls are asynchronous on the handle's stream unless stated otherwise. Calls on one handle must be
+ *    ordered on that stream (they share the handle's scratch).
+ *  - Return values: WHEAD_OK or a negative WHEAD_ERR_* code. A device-side failure (a wait that ran past
+ *    its time limit) is reported by whead_status() and by the next call on the handle.
+ */
+#ifndef WHEAD_H_
+#define WHEAD_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define WHEAD_OK 0
+#define WHEAD_ERR_INVALID_ARG (-1)  /* a null pointer, a size out of range, a misaligned pointer */
+#define WHEAD_ERR_UNSUPPORTED (-2)  /* shape outside what this build handles (see whead_create) */
+#define WHEAD_ERR_CUDA (-3)         /* a CUDA runtime or driver call failed */
+#define WHEAD_ERR_TIMEOUT (-4)      /* a device-side wait gave up after its time limit */
+#define WHEAD_ERR_NO_COOP (-5)      /* the grid cannot be made co-resident (cooperative launch refused) */
+#define WHEAD_ERR_INTERNAL (-6)     /* a device-side consistency check failed */
+
+typedef enum { WHEAD_MARKOV = 0, WHEAD_RECURRENT = 1 } whead_kind;
+
+/* Flags (whead_params.flags). */
+#define WHEAD_FLAG_LOGITS_F32 (1u << 0)      /* out_logits holds fp32 z instead of bf16(z) */
+#define WHEAD_FLAG_FIXED_LATENT (1u << 1)    /* measurement mode: never advance the state (Fig. 13b probe) */
+#define WHEAD_FLAG_FAULT_SKIP_ARRIVAL (1u << 8) /* testing: CTA 0 never arrives at step 0's exchange, so
+                                                   every other CTA's bounded wait runs out */
+
+typedef struct {
+  int32_t kind;        /* WHEAD_MARKOV or WHEAD_RECURRENT */
+  int32_t r;           /* rank: 64, 128, 192 or 256 */
+  int64_t V;           /* vocabulary rows: 1 <= V < 2^24 */
+  const float* A;      /* recurrent only: r x r fp32 row-major, device */
+  const float* c;      /* recurrent only: r fp32, device; NULL means zero */
+  int32_t max_B;       /* largest batch a call will use: 1..16 */
+  int32_t max_gamma;   /* largest number of steps a call will use: 1..64 */
+  void* stream;        /* cudaStream_t for every call on this handle; NULL = legacy default stream */
+  uint32_t flags;      /* WHEAD_FLAG_* */
+  int32_t grid;        /* number of CTAs; 0 = chosen by the planner (at most one per SM) */
+  uint32_t timeout_us; /* limit on every device-side wait; 0 = 1,000,000 us */
+} whead_params;
+
+/* Placement chosen for a batch size (whead_plan_info). Groups are 16 consecutive rows of W. */
+typedef struct {
+  int32_t grid;            /* CTAs (one per SM) */
+  int32_t threads;         /* threads per CTA */
+  int32_t groups_per_cta;  /* 16-row groups each CTA owns */
+  int32_t smem_groups;     /* of which resident in shared memory */
+  int32_t tmem_groups;     /* of which resident in tensor memory */
+  int32_t rf_groups;       /* of which resident in registers */
+  int32_t stream_groups;   /* of which re-read from L2/HBM every step */
+  int32_t smem_bytes;      /* dynamic shared memory per CTA */
+  int32_t tmem_cols;       /* tensor-memory columns allocated per CTA */
+  int32_t sm_count;        /* SMs on the device */
+} whead_plan;
+
+typedef struct whead_s whead_t;
+
+/*
+ * Create a handle for one head (abstract: the serial head of a parallel drafter; Fig. 1: each SM keeps
+ * a shard of W). Validates shapes, queries the device, plans the placement of W over shared memory,
+ * tensor memory and registers for B <= 8 and B <= 16, builds the TMA descriptor of W and allocates the
+ * scratch. W and E: V x r bf16 row-major device arrays, 16-byte aligned. Returns WHEAD_ERR_UNSUPPORTED if
+ * r is not one of 64/128/192/256, if V >= 2^24, if the recurrent head is asked for without A, or if W
+ * cannot be placed for max_B. On success *out owns the scratch; free it with whead_destroy.
+ */
+int whead_create(const void* W, const void* E, const whead_params* params, whead_t** out);
+
+/*
+ * One walk of gamma steps for B independent walks (abstract; Fig. 2; Fig. 8). base: B x gamma x V fp32;
+ * u0: B x r fp32 (the state projected at step 0); T >= 0 (0 = greedy); seed keys the noise.
+ * out_tokens: B x gamma int32. out_logits: NULL, or B x gamma x V bf16 (fp32 with WHEAD_FLAG_LOGITS_F32)
+ * holding z before noise and temperature. Enqueued on the handle's stream.
+ */
+int whead_walk(whead_t* h, const float* base, const float* u0, int32_t B, int32_t gamma, float T,
+               uint64_t seed, int32_t* out_tokens, void* out_logits);
+
+/*
+ * whead_walk with a resume offset: the walk starts at absolute step t0 (which keys the noise) from state
+ * s0 (B x r fp32), and out_state (NULL, or B x gamma x r fp32) receives the state after each step's
+ * advance. Re-running from any step t0 with the state reached there reproduces the remaining tokens,
+ * logits and states bit for bit.
+ */
+int whead_walk_ex(whead_t* h, const float* base, const float* s0, int32_t B, int32_t gamma, float T,
+                  uint64_t seed, int64_t t0, int32_t* out_tokens, void* out_logits, float* out_state);
+
+/*
+ * Synchronous walk on HOST buffers (same arguments as whead_walk, all pointers host memory; pinned
+ * memory gives the fastest copies). Copies base and u0 to handle-owned device staging buffers, runs the
+ * walk and copies the tokens (and logits, if requested) back, then waits for the stream.
+ */
+int whead_walk_host(whead_t* h, const float* base_host, const float* u0_host, int32_t B, int32_t gamma,
+                    float T, uint64_t seed, int32_t* out_tokens_host, void* out_logits_host);
+
+/* Waits for the handle's stream and returns WHEAD_OK or the first device-side error (then clears it). */
+int whead_status(whead_t* h);
+
+/* The placement used for batch size B (1..max_B). */
+int whead_plan_info(const whead_t* h, int32_t B, whead_plan* out);
+
+/* A static description of a return code. */
+const char* whead_strerror(int code);
+
+/* Frees the handle and its scratch. Waits for the handle's stream first. */
+int whead_destroy(whead_t* h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WHEAD_H_ */

@@ -1,0 +1,640 @@
+// walk_kernel.cuh — the walk-resident megakernel for the serial draft head (sm_103a).
+//
+// "Weights That Stay: On-Chip Megakernels for Serial Heads in Speculative Decoding":
+//  - abstract / Fig. 1: each SM keeps a shard of W for the whole walk and only tokens or state cross
+//    between steps;
+//  - Fig. 2: every step projects the state through the same vocabulary projection W and the chosen
+//    token drives the next step;
+//  - Fig. 7: the projection is added to the base logits and rounded once;
+//  - Fig. 8: each CTA scores its rows, packs its local winner, atomically updates the maximum key and an
+//    arrival count, waits for all CTAs and uses the common winner.
+//
+// Design on GB300 (one persistent cooperative CTA of 384 threads per SM):
+//  - W is split into 16-row groups. Each CTA owns `ng` consecutive groups and keeps them in three
+//    on-chip tiers for the whole walk: shared memory (loaded once by TMA with the 128-byte swizzle),
+//    tensor memory (written once with tcgen05.st, read every step with tcgen05.ld) and registers.
+//  - The projection of a group is 16 (r = 256) mma.sync.m16n8k16 bf16 -> fp32 ops whose A operand is
+//    the W group and whose B operand holds the bf16 states of up to 8 walks (two ops for 16 walks).
+//    The k index inside each 64-wide box is permuted so that one 16-byte shared-memory load gives a
+//    thread a full A fragment without bank conflicts; the B fragments use the same permutation, which
+//    makes them 32 contiguous bytes of the state.
+//  - The fp32 result plus the base logit is the selection key (plus Gumbel noise when T > 0); keys are
+//    packed as ord(key) << 32 | (2^32 - 1 - row) so an unsigned 64-bit maximum picks the largest key
+//    and the smallest row on ties.
+//  - Cross-CTA exchange per step: red.max of the packed key into a step slot, then a release add on an
+//    arrival counter; thread 0 of every CTA polls the counter with acquire loads (bounded by a time
+//    limit) and reads the winners.
+//  - State advance on the GPU: Markov u <- E[x]; recurrent h <- tanh(A h + E[x] + c) where each CTA
+//    computes a slice of A h before it arrives and every CTA finishes the update redundantly.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+namespace whead {
+
+constexpr int kThreads = 384;
+constexpr int kWarps = kThreads / 32;
+constexpr int kMaxB = 16;
+constexpr int kMaxGamma = 64;
+constexpr int kMaxWarpGroups = 32;
+constexpr int kGroupRows = 16;
+constexpr int kBoxBytes = kGroupRows * 128;  // one 16-row x 64-element bf16 box
+
+// device status codes (match the public WHEAD_ERR_* values)
+constexpr int kStatusTimeout = -4;
+constexpr int kStatusInternal = -6;
+
+constexpr uint32_t kFlagLogitsF32 = 1u << 0;
+constexpr uint32_t kFlagFixedLatent = 1u << 1;
+constexpr uint32_t kFlagSkipArrival = 1u << 8;
+
+struct WalkArgs {
+  const uint16_t* W;
+  const uint16_t* E;
+  const float* A;
+  const float* c;
+  const float* base;
+  const float* s0;
+  int32_t* tokens;
+  void* logits;
+  float* state;
+  unsigned long long* slots;        // [kMaxGamma][kMaxB] for this call
+  unsigned int* cnt;                // arrival counter for this call
+  unsigned long long* slots_reset;  // the other call parity: cleared during this call
+  unsigned int* cnt_reset;
+  float* ah;                        // [2][kMaxB][r]: slices of A h exchanged between CTAs
+  int* status;
+  int64_t V;
+  int64_t t0;
+  uint64_t seed;
+  uint64_t timeout_ns;
+  float T;
+  int32_t r;
+  int32_t B;
+  int32_t gamma;
+  int32_t kind;
+  uint32_t flags;
+  int32_t ng;        // groups per CTA
+  int32_t n_smem;    // local groups [0, n_smem) live in shared memory
+  int32_t n_tmem;    // [n_smem, n_smem + n_tmem) in tensor memory
+  int32_t n_rf;      // the rest in registers (at most one per warp)
+  uint32_t tmem_cols;
+  int32_t smem_w_bytes;
+  int32_t ra;        // recurrent: rows of A per CTA
+  int32_t wl_count[kWarps];
+  uint8_t wl[kWarps][kMaxWarpGroups];  // CTA-local group indices processed by each warp
+};
+
+// Shared-memory layout after the W tier (byte offsets from the 1024-aligned base).
+struct SmemLayout {
+  int red, win, misc, h, a, total;
+  __host__ __device__ static SmemLayout make(int smem_w_bytes, int B, int r, int ra, bool recurrent) {
+    SmemLayout L;
+    L.red = smem_w_bytes;                       // [kWarps][kMaxB] u64
+    L.win = L.red + kWarps * kMaxB * 8;         // [kMaxB] int32
+    L.misc = L.win + kMaxB * 4;                 // mbarrier u64, tmem addr u32, abort flag u32
+    L.h = L.misc + 16;                          // recurrent: [B][r] fp32
+    L.a = L.h + (recurrent ? B * r * 4 : 0);    // recurrent: [ra][r] fp32
+    L.total = L.a + (recurrent ? ra * r * 4 : 0);
+    return L;
+  }
+};
+
+// TMEM slot i of a CTA: lane quadrant i % 4, column block i / 4; the owning warp must sit on that
+// quadrant (warp % 4), which is how tcgen05.ld restricts lane access.
+__host__ __device__ inline int tmem_slot_warp(int i) { return (i & 3) + 4 * ((i >> 2) % (kWarps / 4)); }
+__host__ __device__ inline int tmem_slot_col(int i, int KB) { return (i >> 2) * 16 * KB; }
+
+// ------------------------------------------------------------------------------------------------
+// small device helpers
+// ------------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t (&a)[16], uint32_t taddr) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]),
+        "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15])
+      : "r"(taddr));
+}
+
+// Waits for this thread's tcgen05.ld; the registers are tied to the wait so no use is scheduled before it.
+__device__ __forceinline__ void tmem_wait_ld(uint32_t (&a)[16]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(a[0]), "+r"(a[1]), "+r"(a[2]), "+r"(a[3]), "+r"(a[4]), "+r"(a[5]), "+r"(a[6]), "+r"(a[7]),
+                 "+r"(a[8]), "+r"(a[9]), "+r"(a[10]), "+r"(a[11]), "+r"(a[12]), "+r"(a[13]), "+r"(a[14]),
+                 "+r"(a[15])
+               :
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&a)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};"
+      :
+      : "r"(taddr), "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(a[4]), "r"(a[5]), "r"(a[6]), "r"(a[7]),
+        "r"(a[8]), "r"(a[9]), "r"(a[10]), "r"(a[11]), "r"(a[12]), "r"(a[13]), "r"(a[14]), "r"(a[15])
+      : "memory");
+}
+
+__device__ __forceinline__ void tmem_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tmem_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Philox4x32 with 10 rounds (Salmon, Moraes, Dror, Shaw, SC'11): multipliers 0xD2511F53 / 0xCD9E8D57,
+// key increments 0x9E3779B9 / 0xBB67AE85 before every round but the first.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 ctr, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int i = 0; i < 10; ++i) {
+    if (i > 0) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint32_t lo0 = 0xD2511F53u * ctr.x, hi0 = __umulhi(0xD2511F53u, ctr.x);
+    const uint32_t lo1 = 0xCD9E8D57u * ctr.z, hi1 = __umulhi(0xCD9E8D57u, ctr.z);
+    ctr = make_uint4(hi1 ^ ctr.y ^ k0, lo1, hi0 ^ ctr.w ^ k1, lo0);
+  }
+  return ctr;
+}
+
+// Standard Gumbel noise for (seed, walk b, absolute step tau, row v): counter (v/4, tau, b, 0), word v%4,
+// U = ((w >> 9) + 0.5) * 2^-23 (exact in fp32), g = -log(-log U).
+__device__ __forceinline__ float gumbel_noise(uint64_t seed, uint32_t b, uint32_t tau, uint32_t v) {
+  const uint4 o = philox4x32_10(make_uint4(v >> 2, tau, b, 0u), (uint32_t)seed, (uint32_t)(seed >> 32));
+  const uint32_t sel = v & 3u;
+  const uint32_t w = sel == 0 ? o.x : sel == 1 ? o.y : sel == 2 ? o.z : o.w;
+  const float u = __fmul_rn(__fadd_rn(__uint2float_rn(w >> 9), 0.5f), 0x1p-23f);
+  return -logf(-logf(u));
+}
+
+// Order-preserving map of an fp32 key to uint32 (negative: bitwise not; else set the sign bit; -0 -> +0),
+// packed above the inverted row so that the unsigned maximum prefers the smaller row on equal keys.
+__device__ __forceinline__ unsigned long long pack_key(float key, uint32_t v) {
+  uint32_t u = __float_as_uint(key);
+  if (u == 0x80000000u) u = 0u;
+  const uint32_t o = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((unsigned long long)o << 32) | (unsigned long long)(0xFFFFFFFFu - v);
+}
+
+// Waits on an mbarrier phase with a time limit; returns false if the limit ran out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t mbar, uint32_t parity, uint64_t timeout_ns) {
+  const uint64_t t_start = globaltimer_ns();
+  while (true) {
+    uint32_t done;
+    asm volatile("{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+                 : "=r"(done)
+                 : "r"(mbar), "r"(parity)
+                 : "memory");
+    if (done) return true;
+    if (globaltimer_ns() - t_start > timeout_ns) return false;
+  }
+}
+
+__device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) { return a > b ? a : b; }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&p);
+}
+
+// Four mma ops of one 64-wide k box. a = [R0 | S0 | R1 | S1]: R rows g, S rows g+8, index 0/1 the two
+// 16-byte chunks (2c, 2c+1) of the box. B fragments: 8 registers per box = 16 contiguous bf16 of the state.
+template <int KB, int NH>
+__device__ __forceinline__ void mma_box(float (&acc)[NH][4], const uint32_t (&a)[16],
+                                        const uint32_t (&bf)[NH][KB][8], int bx) {
+#pragma unroll
+  for (int rho = 0; rho < 2; ++rho) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t a0 = a[8 * rho + 2 * h], a2 = a[8 * rho + 2 * h + 1];
+      const uint32_t a1 = a[8 * rho + 4 + 2 * h], a3 = a[8 * rho + 4 + 2 * h + 1];
+#pragma unroll
+      for (int n = 0; n < NH; ++n)
+        mma_bf16_16816(acc[n], a0, a1, a2, a3, bf[n][bx][4 * rho + 2 * h], bf[n][bx][4 * rho + 2 * h + 1]);
+    }
+  }
+}
+
+// A fragments of box bx of a group read straight from W in global memory (row-major, unswizzled):
+// row g then row g+8, 32 contiguous bytes each (chunks 2c and 2c+1 of the box). Rows >= V read as zero.
+__device__ __forceinline__ void load_box_global(uint32_t (&a)[16], const uint16_t* W, int64_t v0, int64_t V, int r,
+                                                int bx, int c) {
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const int64_t v = v0 + 8 * half;
+    uint4 x0 = make_uint4(0, 0, 0, 0), x1 = make_uint4(0, 0, 0, 0);
+    if (v < V) {
+      const uint4* p = reinterpret_cast<const uint4*>(W + v * r + 64 * bx + 16 * c);
+      x0 = __ldg(p);
+      x1 = __ldg(p + 1);
+    }
+    // layout [R0 | S0 | R1 | S1]
+    a[4 * half + 0] = x0.x; a[4 * half + 1] = x0.y; a[4 * half + 2] = x0.z; a[4 * half + 3] = x0.w;
+    a[8 + 4 * half + 0] = x1.x; a[8 + 4 * half + 1] = x1.y; a[8 + 4 * half + 2] = x1.z; a[8 + 4 * half + 3] = x1.w;
+  }
+}
+
+// Builds the B fragments of walk n from an fp32 state row (global or shared), rounding to bf16.
+template <int KB>
+__device__ __forceinline__ void bfrag_from_f32(uint32_t (&bf)[KB][8], const float* s, int c) {
+#pragma unroll
+  for (int bx = 0; bx < KB; ++bx) {
+    const float4* p = reinterpret_cast<const float4*>(s + 64 * bx + 16 * c);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float4 f = p[i];
+      bf[bx][2 * i] = pack_bf16x2(f.x, f.y);
+      bf[bx][2 * i + 1] = pack_bf16x2(f.z, f.w);
+    }
+  }
+}
+
+template <int KB>
+__device__ __forceinline__ void bfrag_from_bf16_row(uint32_t (&bf)[KB][8], const uint16_t* e, int c) {
+#pragma unroll
+  for (int bx = 0; bx < KB; ++bx) {
+    const uint4* p = reinterpret_cast<const uint4*>(e + 64 * bx + 16 * c);
+    const uint4 x0 = __ldg(p), x1 = __ldg(p + 1);
+    bf[bx][0] = x0.x; bf[bx][1] = x0.y; bf[bx][2] = x0.z; bf[bx][3] = x0.w;
+    bf[bx][4] = x1.x; bf[bx][5] = x1.y; bf[bx][6] = x1.z; bf[bx][7] = x1.w;
+  }
+}
+
+// ------------------------------------------------------------------------------------------------
+// the kernel
+// ------------------------------------------------------------------------------------------------
+template <int KB, int NH>
+__global__ void __launch_bounds__(kThreads, 1)
+    walk_kernel(const __grid_constant__ CUtensorMap tmapW, const __grid_constant__ WalkArgs P) {
+  extern __shared__ uint8_t smem_raw[];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, c = lane & 3;
+  const int G = gridDim.x, cta = blockIdx.x;
+  const int r = P.r, B = P.B, gamma = P.gamma;
+  const int64_t V = P.V;
+  const bool recurrent = P.kind == 1;
+
+  const uint32_t raw_addr = smem_u32(smem_raw);
+  uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
+  const SmemLayout L = SmemLayout::make(P.smem_w_bytes, B, r, P.ra, recurrent);
+  uint8_t* sW = smem;
+  unsigned long long* s_red = reinterpret_cast<unsigned long long*>(smem + L.red);
+  int32_t* s_win = reinterpret_cast<int32_t*>(smem + L.win);
+  unsigned long long* s_mbar = reinterpret_cast<unsigned long long*>(smem + L.misc);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L.misc + 8);
+  volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L.misc + 12);
+  float* s_h = reinterpret_cast<float*>(smem + L.h);
+  float* s_A = reinterpret_cast<float*>(smem + L.a);
+
+  const uint32_t mbar = smem_u32(s_mbar);
+  const int64_t row_base = (int64_t)cta * P.ng * kGroupRows;
+
+  // ---------------- set-up ----------------
+  if (tid == 0) {
+    *s_abort = 0;
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar) : "memory");
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  }
+  if (warp == 0 && P.tmem_cols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(s_tmem)),
+                 "r"(P.tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  // clear the exchange words of the other call parity (the previous call on this stream has finished)
+  if (cta == G - 1) {
+    for (int i = tid; i < kMaxGamma * kMaxB; i += kThreads) P.slots_reset[i] = 0ull;
+    if (tid == 0) *P.cnt_reset = 0u;
+  }
+  tmem_fence_before();
+  __syncthreads();
+  tmem_fence_after();
+  const uint32_t tmem_base = P.tmem_cols ? *s_tmem : 0u;
+
+  // ---------------- entry: load the shard once (Fig. 4: the one-time shard load) ----------------
+  if (tid == 0 && P.n_smem > 0) {
+    const uint32_t bytes = (uint32_t)(P.n_smem * KB * kBoxBytes);
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes) : "memory");
+    const uint32_t dst0 = smem_u32(sW);
+    for (int bx = 0; bx < KB; ++bx) {
+      for (int j = 0; j < P.n_smem; ++j) {
+        const uint32_t dst = dst0 + (uint32_t)(bx * P.n_smem + j) * kBoxBytes;
+        const int x = 64 * bx;
+        const int y = (int)(row_base + (int64_t)kGroupRows * j);
+        asm volatile(
+            "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+            "l"(reinterpret_cast<uint64_t>(&tmapW)), "r"(x), "r"(y), "r"(mbar)
+            : "memory");
+      }
+    }
+  }
+
+  // tensor-memory groups of this warp: global -> registers -> tcgen05.st
+  const uint32_t lane_quadrant = (uint32_t)(32 * (warp & 3)) << 16;
+  for (int e = 0; e < P.wl_count[warp]; ++e) {
+    const int j = P.wl[warp][e];
+    if (j < P.n_smem || j >= P.n_smem + P.n_tmem) continue;
+    const int slot = j - P.n_smem;
+    const uint32_t taddr = tmem_base + lane_quadrant + (uint32_t)tmem_slot_col(slot, KB);
+    const int64_t v0 = row_base + (int64_t)kGroupRows * j + g;
+#pragma unroll
+    for (int bx = 0; bx < KB; ++bx) {
+      uint32_t a[16];
+      load_box_global(a, P.W, v0, V, r, bx, c);
+      tmem_st16(taddr + 16 * bx, a);
+    }
+  }
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+
+  // register-resident group (at most one per warp)
+  uint32_t rfA[(NH == 1) ? KB : 1][16];
+  int rf_group = -1;
+  if constexpr (NH == 1) {
+    for (int e = 0; e < P.wl_count[warp]; ++e) {
+      const int j = P.wl[warp][e];
+      if (j >= P.n_smem + P.n_tmem) rf_group = j;
+    }
+#pragma unroll
+    for (int bx = 0; bx < KB; ++bx) {
+      if (rf_group >= 0) {
+        load_box_global(rfA[bx], P.W, row_base + (int64_t)kGroupRows * rf_group + g, V, r, bx, c);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) rfA[bx][i] = 0u;
+      }
+    }
+  }
+
+  // recurrent head: the initial state and this CTA's rows of A
+  const int a_lo = cta * P.ra;
+  if (recurrent) {
+    for (int i = tid; i < B * r; i += kThreads) s_h[i] = P.s0[i];
+    for (int i = tid; i < P.ra * r; i += kThreads) {
+      const int row = a_lo + i / r;
+      s_A[i] = (row < r) ? P.A[(int64_t)row * r + (i % r)] : 0.f;
+    }
+  }
+
+  // wait for the TMA copies (bounded)
+  bool tma_done = true;
+  if (P.n_smem > 0) {
+    tma_done = mbar_wait_bounded(mbar, 0u, P.timeout_ns);
+    if (!tma_done) {
+      if (tid == 0) atomicCAS(P.status, 0, kStatusTimeout);
+      *s_abort = 1;
+    }
+  }
+  tmem_fence_before();
+  __syncthreads();
+  tmem_fence_after();
+
+  // ---------------- the walk ----------------
+  uint32_t bf[NH][KB][8];
+#pragma unroll
+  for (int h = 0; h < NH; ++h) {
+    const int n = 8 * h + g;
+    if (n < B) {
+      bfrag_from_f32<KB>(bf[h], recurrent ? (s_h + n * r) : (P.s0 + (int64_t)n * r), c);
+    } else {
+#pragma unroll
+      for (int bx = 0; bx < KB; ++bx)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) bf[h][bx][i] = 0u;
+    }
+  }
+
+  const uint32_t sw_base = smem_u32(sW);
+  const uint32_t box_stride = (uint32_t)(P.n_smem * kBoxBytes);
+  const uint32_t off_rho0 = (uint32_t)(((2 * c) ^ g) << 4);
+  const uint32_t off_rho1 = (uint32_t)(((2 * c + 1) ^ g) << 4);
+  const float T = P.T;
+  const bool sampled = T > 0.0f;
+  const bool want_f32 = (P.flags & kFlagLogitsF32) != 0u;
+
+  for (int t = 0; t < gamma; ++t) {
+    if (*s_abort) break;
+    const uint32_t tau = (uint32_t)(P.t0 + t);
+
+    // recurrent: this CTA's slice of A h_t, published with the step's arrival
+    if (recurrent && warp == 0) {
+      for (int p = 0; p < B * P.ra; ++p) {
+        const int n = p / P.ra, i = p % P.ra;
+        if (a_lo + i >= r) continue;
+        float s = 0.f;
+        for (int k = lane; k < r; k += 32) s = fmaf(s_A[i * r + k], s_h[n * r + k], s);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+        if (lane == 0) P.ah[((int64_t)(t & 1) * kMaxB + n) * r + a_lo + i] = s;
+      }
+    }
+
+    unsigned long long best[NH][2];
+#pragma unroll
+    for (int h = 0; h < NH; ++h) best[h][0] = best[h][1] = 0ull;
+
+    for (int e = 0; e < P.wl_count[warp]; ++e) {
+      const int j = P.wl[warp][e];
+      const int64_t va = row_base + (int64_t)kGroupRows * j + g;
+
+      // base logits of this thread's rows and walks, loaded before the projection
+      float bv[NH][4];
+#pragma unroll
+      for (int h = 0; h < NH; ++h)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int64_t v = va + ((q >> 1) << 3);
+          const int n = 8 * h + 2 * c + (q & 1);
+          bv[h][q] = (v < V && n < B) ? __ldg(P.base + ((int64_t)n * gamma + t) * V + v) : 0.f;
+        }
+
+      float acc[2][NH][4];
+#pragma unroll
+      for (int s = 0; s < 2; ++s)
+#pragma unroll
+        for (int h = 0; h < NH; ++h)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) acc[s][h][q] = 0.f;
+
+      if (j < P.n_smem) {
+        const uint32_t row_addr = sw_base + (uint32_t)(kGroupRows * j + g) * 128u;
+#pragma unroll
+        for (int bx = 0; bx < KB; ++bx) {
+          uint32_t a[16];
+          const uint8_t* p = sW + (row_addr - sw_base) + bx * box_stride;
+          const uint4 r0 = *reinterpret_cast<const uint4*>(p + off_rho0);
+          const uint4 s0 = *reinterpret_cast<const uint4*>(p + 1024 + off_rho0);
+          const uint4 r1 = *reinterpret_cast<const uint4*>(p + off_rho1);
+          const uint4 s1 = *reinterpret_cast<const uint4*>(p + 1024 + off_rho1);
+          a[0] = r0.x; a[1] = r0.y; a[2] = r0.z; a[3] = r0.w;
+          a[4] = s0.x; a[5] = s0.y; a[6] = s0.z; a[7] = s0.w;
+          a[8] = r1.x; a[9] = r1.y; a[10] = r1.z; a[11] = r1.w;
+          a[12] = s1.x; a[13] = s1.y; a[14] = s1.z; a[15] = s1.w;
+          mma_box<KB, NH>(acc[bx & 1], a, bf, bx);
+        }
+      } else if (j < P.n_smem + P.n_tmem) {
+        const uint32_t taddr = tmem_base + lane_quadrant + (uint32_t)tmem_slot_col(j - P.n_smem, KB);
+#pragma unroll
+        for (int bx = 0; bx < KB; ++bx) {
+          uint32_t a[16];
+          tmem_ld16(a, taddr + 16 * bx);
+          tmem_wait_ld(a);
+          mma_box<KB, NH>(acc[bx & 1], a, bf, bx);
+        }
+      } else {
+        if constexpr (NH == 1) {
+#pragma unroll
+          for (int bx = 0; bx < KB; ++bx) mma_box<KB, NH>(acc[bx & 1], rfA[bx], bf, bx);
+        }
+      }
+
+      // epilogue: z = p + base (fp32), optional emitted logit, selection key, running maximum
+#pragma unroll
+      for (int h = 0; h < NH; ++h)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int64_t v = va + ((q >> 1) << 3);
+          const int n = 8 * h + 2 * c + (q & 1);
+          if (v < V && n < B) {
+            const float p = __fadd_rn(acc[0][h][q], acc[1][h][q]);
+            const float z = __fadd_rn(p, bv[h][q]);
+            const int64_t oi = ((int64_t)n * gamma + t) * V + v;
+            if (P.logits) {
+              if (want_f32) reinterpret_cast<float*>(P.logits)[oi] = z;
+              else reinterpret_cast<__nv_bfloat16*>(P.logits)[oi] = __float2bfloat16_rn(z);
+            }
+            float key = z;
+            if (sampled) key = __fadd_rn(__fdiv_rn(z, T), gumbel_noise(P.seed, (uint32_t)n, tau, (uint32_t)v));
+            best[h][q & 1] = umax64(best[h][q & 1], pack_key(key, (uint32_t)v));
+          }
+        }
+    }
+
+    // warp maximum over the 8 row positions g; lanes 0..3 then hold walks 8h + 2c and 8h + 2c + 1
+#pragma unroll
+    for (int h = 0; h < NH; ++h)
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {
+        unsigned long long k = best[h][i];
+        k = umax64(k, __shfl_xor_sync(0xffffffffu, k, 4));
+        k = umax64(k, __shfl_xor_sync(0xffffffffu, k, 8));
+        k = umax64(k, __shfl_xor_sync(0xffffffffu, k, 16));
+        const int n = 8 * h + 2 * c + i;
+        if (g == 0 && n < B) s_red[warp * kMaxB + n] = k;
+      }
+    __syncthreads();
+
+    // exchange (Fig. 8): CTA winner -> red.max into the step slot, release arrival, bounded acquire poll
+    if (warp == 0) {
+      unsigned long long k = 0ull;
+      if (lane < B)
+        for (int w = 0; w < kWarps; ++w) k = umax64(k, s_red[w * kMaxB + lane]);
+      unsigned long long* slot = P.slots + (int64_t)t * kMaxB;
+      for (int n = 0; n < B; ++n) {
+        const unsigned long long kn = __shfl_sync(0xffffffffu, k, n);
+        if (lane == 0 && kn != 0ull) asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(slot + n), "l"(kn) : "memory");
+      }
+      if (lane == 0) {
+        const bool skip = (P.flags & kFlagSkipArrival) && cta == 0 && t == 0;
+        if (!skip) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(P.cnt) : "memory");
+        const unsigned int target = (unsigned int)(t + 1) * (unsigned int)G;
+        const uint64_t t_start = globaltimer_ns();
+        uint32_t spins = 0;
+        while (true) {
+          unsigned int now;
+          asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(now) : "l"(P.cnt) : "memory");
+          if (now >= target) break;
+          if ((++spins & 31u) == 0u && globaltimer_ns() - t_start > P.timeout_ns) {
+            atomicCAS(P.status, 0, kStatusTimeout);
+            *s_abort = 1;
+            break;
+          }
+        }
+        for (int n = 0; n < B; ++n) {
+          unsigned long long kn;
+          asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(kn) : "l"(slot + n) : "memory");
+          const uint32_t x = 0xFFFFFFFFu - (uint32_t)(kn & 0xFFFFFFFFull);
+          s_win[n] = (int32_t)x;
+          if (cta == 0 && !*s_abort) P.tokens[(int64_t)n * gamma + t] = (int32_t)x;
+        }
+      }
+    }
+    __syncthreads();
+    if (*s_abort) break;
+
+    // winners must be rows of W (a failed exchange would show up here)
+    bool bad = false;
+    for (int n = 0; n < B; ++n) bad |= (s_win[n] < 0 || (int64_t)s_win[n] >= V);
+    if (bad) {
+      if (tid == 0) atomicCAS(P.status, 0, kStatusInternal);
+      break;
+    }
+
+    // ---------------- state advance ----------------
+    if (P.flags & kFlagFixedLatent) continue;
+    if (!recurrent) {
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        const int n = 8 * h + g;
+        if (n < B) bfrag_from_bf16_row<KB>(bf[h], P.E + (int64_t)s_win[n] * r, c);
+      }
+      if (cta == 0 && P.state) {
+        for (int i = tid; i < B * r; i += kThreads) {
+          const int n = i / r, k = i % r;
+          const uint32_t bits = (uint32_t)P.E[(int64_t)s_win[n] * r + k] << 16;
+          P.state[((int64_t)n * gamma + t) * r + k] = __uint_as_float(bits);
+        }
+      }
+    } else {
+      const float* ah = P.ah + (int64_t)(t & 1) * kMaxB * r;
+      for (int i = tid; i < B * r; i += kThreads) {
+        const int n = i / r, k = i % r;
+        const float e = __uint_as_float((uint32_t)P.E[(int64_t)s_win[n] * r + k] << 16);
+        float pre = __fadd_rn(__ldcg(ah + n * r + k), e);
+        if (P.c) pre = __fadd_rn(pre, P.c[k]);
+        s_h[i] = tanhf(pre);
+      }
+      __syncthreads();
+#pragma unroll
+      for (int h = 0; h < NH; ++h) {
+        const int n = 8 * h + g;
+        if (n < B) bfrag_from_f32<KB>(bf[h], s_h + n * r, c);
+      }
+      if (cta == 0 && P.state) {
+        for (int i = tid; i < B * r; i += kThreads) {
+          const int n = i / r, k = i % r;
+          P.state[((int64_t)n * gamma + t) * r + k] = s_h[i];
+        }
+      }
+    }
+  }
+
+  // ---------------- exit ----------------
+  // copies still in flight after a timed-out wait must land before the CTA's shared memory is released
+  if (!tma_done) (void)mbar_wait_bounded(mbar, 0u, P.timeout_ns);
+  tmem_fence_before();
+  __syncthreads();
+  tmem_fence_after();
+  if (warp == 0 && P.tmem_cols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base), "r"(P.tmem_cols) : "memory");
+  }
+}
+
+}  // namespace whead

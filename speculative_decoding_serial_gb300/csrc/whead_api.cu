@@ -1,0 +1,423 @@
+// whead_api.cu — C ABI, placement planner and launch of the walk-resident serial draft head.
+//
+// "Weights That Stay: On-Chip Megakernels for Serial Heads in Speculative Decoding", Fig. 1: full or
+// partial residency of W across the GPU's memory tiers. The planner below splits W into 16-row groups,
+// gives each SM an equal run of groups and places them in shared memory, tensor memory and registers.
+#include "../../include/whead.h"
+#include "walk_kernel.cuh"
+
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+using namespace whead;
+
+namespace {
+
+struct Plan {
+  bool ok = false;
+  int G = 0, ng = 0, n_smem = 0, n_tmem = 0, n_rf = 0, n_stream = 0;
+  uint32_t tmem_cols = 0;
+  int smem_bytes = 0, smem_w_bytes = 0, ra = 0, Bcap = 0;
+  int32_t wl_count[kWarps] = {};
+  uint8_t wl[kWarps][kMaxWarpGroups] = {};
+};
+
+struct Scratch {
+  unsigned long long* slots;  // [2][kMaxGamma * kMaxB]
+  unsigned int* cnt;          // two counters, 128 bytes apart
+  float* ah;                  // [2][kMaxB][r]
+  int* status;
+};
+
+}  // namespace
+
+struct whead_s {
+  int device = 0;
+  cudaStream_t stream = nullptr;
+  whead_params p{};
+  const uint16_t* W = nullptr;
+  const uint16_t* E = nullptr;
+  CUtensorMap tmap{};
+  int sm_count = 0, smem_optin = 0;
+  Plan plan[2];  // walks <= 8, walks <= 16
+  void* scratch_block = nullptr;
+  Scratch s{};
+  uint32_t parity = 0;
+  // host-call staging
+  float* d_base = nullptr;
+  float* d_u0 = nullptr;
+  int32_t* d_tok = nullptr;
+  void* d_logits = nullptr;
+};
+
+namespace {
+
+int kb_of(int r) { return r / 64; }
+
+// Planner: number of CTAs, groups per CTA and their tier; per-warp work lists balanced over the four
+// SM sub-partitions (warp % 4), which each own one tensor core and one quarter of tensor memory.
+Plan make_plan(int64_t V, int r, int kind, int Bcap, int NH, int sm_count, int smem_optin, int grid_req) {
+  Plan P;
+  const int KB = kb_of(r);
+  const int64_t ngt = (V + kGroupRows - 1) / kGroupRows;
+  const int64_t group_bytes = (int64_t)KB * kBoxBytes;
+  const bool recurrent = kind == WHEAD_RECURRENT;
+  const int tmem_max = 128 / KB;
+  const int rf_max = (NH == 1) ? kWarps : 0;
+
+  auto fits = [&](int G, Plan& out) -> bool {
+    const int64_t ng64 = (ngt + G - 1) / G;
+    if (ng64 > 255) return false;
+    const int ng = (int)ng64;
+    const int ra = recurrent ? (r + G - 1) / G : 0;
+    const SmemLayout L0 = SmemLayout::make(0, Bcap, r, ra, recurrent);
+    const int64_t fixed = 1024 + L0.total;
+    const int64_t smem_groups_max = std::max<int64_t>(0, (smem_optin - fixed) / group_bytes);
+    int n_smem = (int)std::min<int64_t>(ng, smem_groups_max);
+    int rem = ng - n_smem;
+    int n_tmem = std::min(rem, tmem_max);
+    rem -= n_tmem;
+    int n_rf = std::min(rem, rf_max);
+    rem -= n_rf;
+    if (rem > 0) return false;
+    out = Plan();
+    out.G = G;
+    out.ng = ng;
+    out.n_smem = n_smem;
+    out.n_tmem = n_tmem;
+    out.n_rf = n_rf;
+    out.ra = ra;
+    out.Bcap = Bcap;
+    out.smem_w_bytes = (int)(n_smem * group_bytes);
+    out.smem_bytes = (int)(1024 + SmemLayout::make(out.smem_w_bytes, Bcap, r, ra, recurrent).total);
+    if (n_tmem > 0) {
+      const int cols = ((n_tmem - 1) / 4 + 1) * 16 * KB;
+      uint32_t pw = 32;
+      while ((int)pw < cols) pw <<= 1;
+      out.tmem_cols = pw;
+    }
+    // work lists
+    int load[kWarps] = {};
+    int sp_load[4] = {};
+    auto push = [&](int w, int j) -> bool {
+      if (out.wl_count[w] >= kMaxWarpGroups) return false;
+      out.wl[w][out.wl_count[w]++] = (uint8_t)j;
+      load[w]++;
+      sp_load[w & 3]++;
+      return true;
+    };
+    for (int i = 0; i < n_tmem; ++i)
+      if (!push(tmem_slot_warp(i), n_smem + i)) return false;
+    bool has_rf[kWarps] = {};
+    for (int i = 0; i < n_rf; ++i) {
+      int best = -1;
+      for (int w = 0; w < kWarps; ++w)
+        if (!has_rf[w] && (best < 0 || sp_load[w & 3] < sp_load[best & 3] ||
+                           (sp_load[w & 3] == sp_load[best & 3] && load[w] < load[best])))
+          best = w;
+      has_rf[best] = true;
+      if (!push(best, n_smem + n_tmem + i)) return false;
+    }
+    for (int j = 0; j < n_smem; ++j) {
+      int q = 0;
+      for (int k = 1; k < 4; ++k)
+        if (sp_load[k] < sp_load[q]) q = k;
+      int best = q;
+      for (int w = q; w < kWarps; w += 4)
+        if (load[w] < load[best]) best = w;
+      if (!push(best, j)) return false;
+    }
+    out.ok = true;
+    return true;
+  };
+
+  int G;
+  if (grid_req > 0) {
+    G = std::min(grid_req, sm_count);
+    if (!fits(G, P)) P.ok = false;
+    return P;
+  }
+  // few CTAs for small heads (cheaper exchange), more until the shard fits on chip
+  const int64_t target = 96 * 1024;
+  G = (int)std::min<int64_t>(sm_count, std::max<int64_t>(1, (ngt * group_bytes + target - 1) / target));
+  for (; G <= sm_count; ++G)
+    if (fits(G, P)) return P;
+  P.ok = false;
+  return P;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+template <int KB, int NH>
+int launch_t(whead_t* h, const Plan& pl, const WalkArgs& a) {
+  auto fn = walk_kernel<KB, NH>;
+  static int attr_bytes = 0;  // largest dynamic shared memory size granted so far (per instantiation)
+  if (pl.smem_bytes > attr_bytes) {
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, h->smem_optin) != cudaSuccess)
+      return WHEAD_ERR_CUDA;
+    attr_bytes = h->smem_optin;
+  }
+  void* args[] = {(void*)&h->tmap, (void*)&a};
+  cudaError_t e = cudaLaunchCooperativeKernel((const void*)fn, dim3(pl.G), dim3(kThreads), args, (size_t)pl.smem_bytes,
+                                              h->stream);
+  if (e == cudaErrorCooperativeLaunchTooLarge) {
+    (void)cudaGetLastError();
+    return WHEAD_ERR_NO_COOP;
+  }
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return WHEAD_ERR_CUDA;
+  }
+  return WHEAD_OK;
+}
+
+int launch(whead_t* h, const Plan& pl, const WalkArgs& a, int NH) {
+  const int KB = kb_of(h->p.r);
+  switch (KB * 2 + (NH - 1)) {
+    case 2: return launch_t<1, 1>(h, pl, a);
+    case 3: return launch_t<1, 2>(h, pl, a);
+    case 4: return launch_t<2, 1>(h, pl, a);
+    case 5: return launch_t<2, 2>(h, pl, a);
+    case 6: return launch_t<3, 1>(h, pl, a);
+    case 7: return launch_t<3, 2>(h, pl, a);
+    case 8: return launch_t<4, 1>(h, pl, a);
+    case 9: return launch_t<4, 2>(h, pl, a);
+    default: return WHEAD_ERR_UNSUPPORTED;
+  }
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+
+extern "C" {
+
+const char* whead_strerror(int code) {
+  switch (code) {
+    case WHEAD_OK: return "ok";
+    case WHEAD_ERR_INVALID_ARG: return "invalid argument";
+    case WHEAD_ERR_UNSUPPORTED: return "unsupported shape or configuration";
+    case WHEAD_ERR_CUDA: return "CUDA call failed";
+    case WHEAD_ERR_TIMEOUT: return "a device-side wait ran past its time limit";
+    case WHEAD_ERR_NO_COOP: return "grid cannot be co-resident (cooperative launch refused)";
+    case WHEAD_ERR_INTERNAL: return "device-side consistency check failed";
+    default: return "unknown error";
+  }
+}
+
+int whead_create(const void* W, const void* E, const whead_params* params, whead_t** out) {
+  if (!W || !E || !params || !out) return WHEAD_ERR_INVALID_ARG;
+  *out = nullptr;
+  const whead_params& p = *params;
+  if (p.kind != WHEAD_MARKOV && p.kind != WHEAD_RECURRENT) return WHEAD_ERR_INVALID_ARG;
+  if (p.V < 1 || p.max_B < 1 || p.max_B > kMaxB || p.max_gamma < 1 || p.max_gamma > kMaxGamma)
+    return WHEAD_ERR_INVALID_ARG;
+  if (p.V >= (int64_t)1 << 24) return WHEAD_ERR_UNSUPPORTED;
+  if (p.r != 64 && p.r != 128 && p.r != 192 && p.r != 256) return WHEAD_ERR_UNSUPPORTED;
+  if (p.kind == WHEAD_RECURRENT && !p.A) return WHEAD_ERR_UNSUPPORTED;
+  if (!aligned16(W) || !aligned16(E)) return WHEAD_ERR_INVALID_ARG;
+
+  whead_t* h = new (std::nothrow) whead_s();
+  if (!h) return WHEAD_ERR_INVALID_ARG;
+  h->p = p;
+  h->W = static_cast<const uint16_t*>(W);
+  h->E = static_cast<const uint16_t*>(E);
+  h->stream = static_cast<cudaStream_t>(p.stream);
+  if (h->p.timeout_us == 0) h->p.timeout_us = 1000000u;
+  auto fail = [&](int code) {
+    whead_destroy(h);
+    return code;
+  };
+  if (cudaGetDevice(&h->device) != cudaSuccess) return fail(WHEAD_ERR_CUDA);
+  if (cudaDeviceGetAttribute(&h->sm_count, cudaDevAttrMultiProcessorCount, h->device) != cudaSuccess)
+    return fail(WHEAD_ERR_CUDA);
+  if (cudaDeviceGetAttribute(&h->smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, h->device) != cudaSuccess)
+    return fail(WHEAD_ERR_CUDA);
+  int coop = 0;
+  if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->device) != cudaSuccess || !coop)
+    return fail(WHEAD_ERR_NO_COOP);
+
+  // placements: walks <= 8 (one n8 half) and, if asked for, walks <= 16
+  h->plan[0] = make_plan(p.V, p.r, p.kind, std::min(p.max_B, 8), 1, h->sm_count, h->smem_optin, p.grid);
+  if (!h->plan[0].ok) return fail(WHEAD_ERR_UNSUPPORTED);
+  if (p.max_B > 8) {
+    h->plan[1] = make_plan(p.V, p.r, p.kind, p.max_B, 2, h->sm_count, h->smem_optin, p.grid);
+    if (!h->plan[1].ok) return fail(WHEAD_ERR_UNSUPPORTED);
+  }
+
+  // TMA descriptor of W: 2-D (r elements inner, V rows), 64 x 16 boxes, 128-byte swizzle, zero fill
+  auto encode = get_encode();
+  if (!encode) return fail(WHEAD_ERR_CUDA);
+  cuuint64_t gdim[2] = {(cuuint64_t)p.r, (cuuint64_t)p.V};
+  cuuint64_t gstride[1] = {(cuuint64_t)p.r * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)kGroupRows};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult cr = encode(&h->tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W), gdim, gstride, box, estride,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (cr != CUDA_SUCCESS) return fail(WHEAD_ERR_CUDA);
+
+  // scratch: exchange slots (two parities), two counters on their own lines, A h slices, status word
+  const size_t slots_bytes = 2 * (size_t)kMaxGamma * kMaxB * 8;
+  const size_t cnt_bytes = 256;
+  const size_t ah_bytes = 2 * (size_t)kMaxB * p.r * 4;
+  const size_t total = slots_bytes + cnt_bytes + ah_bytes + 256;
+  if (cudaMalloc(&h->scratch_block, total) != cudaSuccess) return fail(WHEAD_ERR_CUDA);
+  if (cudaMemset(h->scratch_block, 0, total) != cudaSuccess) return fail(WHEAD_ERR_CUDA);
+  uint8_t* b = static_cast<uint8_t*>(h->scratch_block);
+  h->s.slots = reinterpret_cast<unsigned long long*>(b);
+  h->s.cnt = reinterpret_cast<unsigned int*>(b + slots_bytes);
+  h->s.ah = reinterpret_cast<float*>(b + slots_bytes + cnt_bytes);
+  h->s.status = reinterpret_cast<int*>(b + slots_bytes + cnt_bytes + ah_bytes);
+  *out = h;
+  return WHEAD_OK;
+}
+
+int whead_walk_ex(whead_t* h, const float* base, const float* s0, int32_t B, int32_t gamma, float T, uint64_t seed,
+                  int64_t t0, int32_t* out_tokens, void* out_logits, float* out_state) {
+  if (!h || !base || !s0 || !out_tokens) return WHEAD_ERR_INVALID_ARG;
+  if (B < 1 || B > h->p.max_B || gamma < 1 || gamma > h->p.max_gamma || t0 < 0) return WHEAD_ERR_INVALID_ARG;
+  if (!(T >= 0.0f) || T != T || T > 3.0e38f) return WHEAD_ERR_INVALID_ARG;
+  if (!aligned16(s0) || (out_state && !aligned16(out_state))) return WHEAD_ERR_INVALID_ARG;
+  const int NH = B <= 8 ? 1 : 2;
+  const Plan& pl = h->plan[NH - 1];
+  if (!pl.ok) return WHEAD_ERR_UNSUPPORTED;
+
+  WalkArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.W = h->W;
+  a.E = h->E;
+  a.A = h->p.A;
+  a.c = h->p.c;
+  a.base = base;
+  a.s0 = s0;
+  a.tokens = out_tokens;
+  a.logits = out_logits;
+  a.state = out_state;
+  const uint32_t par = h->parity & 1u;
+  a.slots = h->s.slots + (size_t)par * kMaxGamma * kMaxB;
+  a.cnt = h->s.cnt + par * 32;
+  a.slots_reset = h->s.slots + (size_t)(par ^ 1u) * kMaxGamma * kMaxB;
+  a.cnt_reset = h->s.cnt + (par ^ 1u) * 32;
+  a.ah = h->s.ah;
+  a.status = h->s.status;
+  a.V = h->p.V;
+  a.t0 = t0;
+  a.seed = seed;
+  a.timeout_ns = (uint64_t)h->p.timeout_us * 1000ull;
+  a.T = T;
+  a.r = h->p.r;
+  a.B = B;
+  a.gamma = gamma;
+  a.kind = h->p.kind;
+  a.flags = h->p.flags;
+  a.ng = pl.ng;
+  a.n_smem = pl.n_smem;
+  a.n_tmem = pl.n_tmem;
+  a.n_rf = pl.n_rf;
+  a.tmem_cols = pl.tmem_cols;
+  a.smem_w_bytes = pl.smem_w_bytes;
+  a.ra = pl.ra;
+  std::memcpy(a.wl_count, pl.wl_count, sizeof(a.wl_count));
+  std::memcpy(a.wl, pl.wl, sizeof(a.wl));
+  const int rc = launch(h, pl, a, NH);
+  if (rc == WHEAD_OK) h->parity ^= 1u;
+  return rc;
+}
+
+int whead_walk(whead_t* h, const float* base, const float* u0, int32_t B, int32_t gamma, float T, uint64_t seed,
+               int32_t* out_tokens, void* out_logits) {
+  return whead_walk_ex(h, base, u0, B, gamma, T, seed, 0, out_tokens, out_logits, nullptr);
+}
+
+int whead_walk_host(whead_t* h, const float* base_host, const float* u0_host, int32_t B, int32_t gamma, float T,
+                    uint64_t seed, int32_t* out_tokens_host, void* out_logits_host) {
+  if (!h || !base_host || !u0_host || !out_tokens_host) return WHEAD_ERR_INVALID_ARG;
+  if (B < 1 || B > h->p.max_B || gamma < 1 || gamma > h->p.max_gamma) return WHEAD_ERR_INVALID_ARG;
+  const size_t nbase = (size_t)B * gamma * h->p.V;
+  const size_t logit_elem = (h->p.flags & WHEAD_FLAG_LOGITS_F32) ? 4 : 2;
+  if (!h->d_base) {
+    const size_t cap = (size_t)h->p.max_B * h->p.max_gamma * h->p.V;
+    if (cudaMalloc(&h->d_base, cap * 4) != cudaSuccess) return WHEAD_ERR_CUDA;
+    if (cudaMalloc(&h->d_u0, (size_t)h->p.max_B * h->p.r * 4) != cudaSuccess) return WHEAD_ERR_CUDA;
+    if (cudaMalloc(&h->d_tok, (size_t)h->p.max_B * h->p.max_gamma * 4) != cudaSuccess) return WHEAD_ERR_CUDA;
+  }
+  if (out_logits_host && !h->d_logits) {
+    const size_t cap = (size_t)h->p.max_B * h->p.max_gamma * h->p.V;
+    if (cudaMalloc(&h->d_logits, cap * logit_elem) != cudaSuccess) return WHEAD_ERR_CUDA;
+  }
+  if (cudaMemcpyAsync(h->d_base, base_host, nbase * 4, cudaMemcpyHostToDevice, h->stream) != cudaSuccess)
+    return WHEAD_ERR_CUDA;
+  if (cudaMemcpyAsync(h->d_u0, u0_host, (size_t)B * h->p.r * 4, cudaMemcpyHostToDevice, h->stream) != cudaSuccess)
+    return WHEAD_ERR_CUDA;
+  int rc = whead_walk(h, h->d_base, h->d_u0, B, gamma, T, seed, h->d_tok, out_logits_host ? h->d_logits : nullptr);
+  if (rc != WHEAD_OK) return rc;
+  if (cudaMemcpyAsync(out_tokens_host, h->d_tok, (size_t)B * gamma * 4, cudaMemcpyDeviceToHost, h->stream) !=
+      cudaSuccess)
+    return WHEAD_ERR_CUDA;
+  if (out_logits_host &&
+      cudaMemcpyAsync(out_logits_host, h->d_logits, nbase * logit_elem, cudaMemcpyDeviceToHost, h->stream) != cudaSuccess)
+    return WHEAD_ERR_CUDA;
+  if (cudaStreamSynchronize(h->stream) != cudaSuccess) return WHEAD_ERR_CUDA;
+  return WHEAD_OK;
+}
+
+int whead_status(whead_t* h) {
+  if (!h) return WHEAD_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(h->stream) != cudaSuccess) return WHEAD_ERR_CUDA;
+  int st = 0;
+  if (cudaMemcpy(&st, h->s.status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return WHEAD_ERR_CUDA;
+  if (st != 0) {
+    const int zero = 0;
+    if (cudaMemcpy(h->s.status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return WHEAD_ERR_CUDA;
+  }
+  return st;
+}
+
+int whead_plan_info(const whead_t* h, int32_t B, whead_plan* out) {
+  if (!h || !out || B < 1 || B > h->p.max_B) return WHEAD_ERR_INVALID_ARG;
+  const Plan& pl = h->plan[B <= 8 ? 0 : 1];
+  if (!pl.ok) return WHEAD_ERR_UNSUPPORTED;
+  out->grid = pl.G;
+  out->threads = kThreads;
+  out->groups_per_cta = pl.ng;
+  out->smem_groups = pl.n_smem;
+  out->tmem_groups = pl.n_tmem;
+  out->rf_groups = pl.n_rf;
+  out->stream_groups = pl.n_stream;
+  out->smem_bytes = pl.smem_bytes;
+  out->tmem_cols = (int32_t)pl.tmem_cols;
+  out->sm_count = h->sm_count;
+  return WHEAD_OK;
+}
+
+int whead_destroy(whead_t* h) {
+  if (!h) return WHEAD_ERR_INVALID_ARG;
+  int rc = WHEAD_OK;
+  if (h->scratch_block || h->d_base) {
+    if (cudaStreamSynchronize(h->stream) != cudaSuccess) rc = WHEAD_ERR_CUDA;
+  }
+  if (h->scratch_block) cudaFree(h->scratch_block);
+  if (h->d_base) cudaFree(h->d_base);
+  if (h->d_u0) cudaFree(h->d_u0);
+  if (h->d_tok) cudaFree(h->d_tok);
+  if (h->d_logits) cudaFree(h->d_logits);
+  delete h;
+  return rc;
+}
+
+}  // extern "C"

@@ -1,0 +1,176 @@
+"""Python binding of the whead C ABI (argument marshalling only).
+
+Every step of the walk runs in the CUDA library libwhead.so; this module only converts torch tensors to
+device pointers and the current CUDA stream to a cudaStream_t. There is no fallback: if the library is
+missing or was not built for this machine, loading raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+MARKOV = 0
+RECURRENT = 1
+
+FLAG_LOGITS_F32 = 1 << 0
+FLAG_FIXED_LATENT = 1 << 1
+FLAG_FAULT_SKIP_ARRIVAL = 1 << 8
+
+OK = 0
+ERR_INVALID_ARG = -1
+ERR_UNSUPPORTED = -2
+ERR_CUDA = -3
+ERR_TIMEOUT = -4
+ERR_NO_COOP = -5
+ERR_INTERNAL = -6
+
+# Every symbol include/whead.h declares.
+EXPORTS = ("whead_create", "whead_walk", "whead_walk_ex", "whead_walk_host", "whead_status",
+           "whead_plan_info", "whead_strerror", "whead_destroy")
+
+
+class WheadParams(ctypes.Structure):
+    _fields_ = [("kind", ctypes.c_int32), ("r", ctypes.c_int32), ("V", ctypes.c_int64),
+                ("A", ctypes.c_void_p), ("c", ctypes.c_void_p), ("max_B", ctypes.c_int32),
+                ("max_gamma", ctypes.c_int32), ("stream", ctypes.c_void_p), ("flags", ctypes.c_uint32),
+                ("grid", ctypes.c_int32), ("timeout_us", ctypes.c_uint32)]
+
+
+class WheadPlan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("grid", "threads", "groups_per_cta", "smem_groups", "tmem_groups",
+                                              "rf_groups", "stream_groups", "smem_bytes", "tmem_cols", "sm_count")]
+
+
+class WheadError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {strerror(code)} ({code})")
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False) -> ctypes.CDLL:
+    """Load libwhead.so (optionally building it first). Raises if it is not there."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if build_if_missing and _build.needs_build():
+        _build.build()
+    if not os.path.exists(path):
+        raise ImportError(f"libwhead.so is not built ({path}); run speculative_decoding_serial_gb300.build.build()")
+    L = ctypes.CDLL(path)
+    vp, i32, i64, u64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float
+    L.whead_create.argtypes = [vp, vp, ctypes.POINTER(WheadParams), ctypes.POINTER(vp)]
+    L.whead_walk.argtypes = [vp, vp, vp, i32, i32, f32, u64, vp, vp]
+    L.whead_walk_ex.argtypes = [vp, vp, vp, i32, i32, f32, u64, i64, vp, vp, vp]
+    L.whead_walk_host.argtypes = [vp, vp, vp, i32, i32, f32, u64, vp, vp]
+    L.whead_status.argtypes = [vp]
+    L.whead_plan_info.argtypes = [vp, i32, ctypes.POINTER(WheadPlan)]
+    L.whead_strerror.argtypes = [ctypes.c_int]
+    L.whead_strerror.restype = ctypes.c_char_p
+    L.whead_destroy.argtypes = [vp]
+    for name in ("whead_create", "whead_walk", "whead_walk_ex", "whead_walk_host", "whead_status",
+                 "whead_plan_info", "whead_destroy"):
+        getattr(L, name).restype = ctypes.c_int
+    _lib = L
+    return L
+
+
+def strerror(code: int) -> str:
+    return load().whead_strerror(int(code)).decode()
+
+
+def _check(code: int, what: str):
+    if code != OK:
+        raise WheadError(code, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    import torch
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+class Head:
+    """A serial draft head whose projection W stays on chip for each walk.
+
+    W, E: (V, r) torch.bfloat16 CUDA tensors (borrowed: keep them alive and unchanged). For the recurrent
+    head pass A (r, r) float32 and optionally c (r,) float32. All calls go to `stream` (default: the
+    current torch stream at construction).
+    """
+
+    def __init__(self, W, E, *, kind=MARKOV, A=None, c=None, max_B=1, max_gamma=16, stream=None, flags=0,
+                 grid=0, timeout_us=0):
+        import torch
+        L = load()
+        assert W.is_cuda and W.dtype == torch.bfloat16 and W.is_contiguous() and W.dim() == 2
+        assert E.shape == W.shape and E.dtype == torch.bfloat16 and E.is_contiguous()
+        self.V, self.r = int(W.shape[0]), int(W.shape[1])
+        self.kind, self.flags = int(kind), int(flags)
+        self._keep = (W, E, A, c)
+        self._stream = torch.cuda.current_stream() if stream is None else stream
+        p = WheadParams(kind=self.kind, r=self.r, V=self.V, A=_ptr(A), c=_ptr(c), max_B=int(max_B),
+                        max_gamma=int(max_gamma), stream=ctypes.c_void_p(self._stream.cuda_stream),
+                        flags=self.flags, grid=int(grid), timeout_us=int(timeout_us))
+        h = ctypes.c_void_p()
+        _check(L.whead_create(_ptr(W), _ptr(E), ctypes.byref(p), ctypes.byref(h)), "whead_create")
+        self._h = h
+        self.max_B, self.max_gamma = int(max_B), int(max_gamma)
+
+    def walk(self, base, u0, *, T=0.0, seed=0, out_tokens=None, out_logits=None):
+        """base (B, gamma, V) float32, u0 (B, r) float32 CUDA tensors. Returns int32 tokens (B, gamma)."""
+        return self.walk_ex(base, u0, T=T, seed=seed, t0=0, out_tokens=out_tokens, out_logits=out_logits)
+
+    def walk_ex(self, base, s0, *, T=0.0, seed=0, t0=0, out_tokens=None, out_logits=None, out_state=None):
+        import torch
+        B, gamma, V = base.shape
+        assert V == self.V and s0.shape == (B, self.r)
+        assert base.dtype == torch.float32 and s0.dtype == torch.float32
+        assert base.is_contiguous() and s0.is_contiguous()
+        if out_tokens is None:
+            out_tokens = torch.empty((B, gamma), dtype=torch.int32, device=base.device)
+        _check(load().whead_walk_ex(self._h, _ptr(base), _ptr(s0), B, gamma, float(T), int(seed) & (2**64 - 1),
+                                    int(t0), _ptr(out_tokens), _ptr(out_logits), _ptr(out_state)), "whead_walk_ex")
+        return out_tokens
+
+    def walk_host(self, base, u0, *, T=0.0, seed=0, out_tokens=None, out_logits=None):
+        """Synchronous walk on host (CPU, ideally pinned) torch tensors; copies are inside the call."""
+        import torch
+        B, gamma, V = base.shape
+        assert V == self.V and not base.is_cuda and not u0.is_cuda
+        if out_tokens is None:
+            out_tokens = torch.empty((B, gamma), dtype=torch.int32)
+        _check(load().whead_walk_host(self._h, _ptr(base), _ptr(u0), B, gamma, float(T), int(seed) & (2**64 - 1),
+                                      _ptr(out_tokens), _ptr(out_logits)), "whead_walk_host")
+        return out_tokens
+
+    def status(self) -> int:
+        return int(load().whead_status(self._h))
+
+    def plan(self, B: int = 1) -> dict:
+        pl = WheadPlan()
+        _check(load().whead_plan_info(self._h, int(B), ctypes.byref(pl)), "whead_plan_info")
+        return {n: int(getattr(pl, n)) for n, _ in WheadPlan._fields_}
+
+    def close(self):
+        if getattr(self, "_h", None):
+            load().whead_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -1,0 +1,190 @@
+"""GPU parity: the CUDA walk (through the C ABI) against the CPU oracle on the same seeded inputs.
+
+Covers the Fig. 2 walk structure ("Weights That Stay", Fig. 2), the single rounding of base-added
+logits (Fig. 7), the cross-CTA selection (Fig. 8), Markov and recurrent heads (abstract), sampling at
+T > 0, ragged vocabularies, several ranks and batch sizes, resume from any step, determinism, the
+host-buffer entry point and the bounded-wait failure path.
+"""
+import numpy as np
+import pytest
+
+import whead_inputs as I
+from oracle import oracle as O
+from parity_helpers import GAP, LOGIT_TOL, bf16_to_f32, check_walk, run_gpu, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def torch_cuda():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.fail("a GPU test ran without a CUDA device")
+    from speculative_decoding_serial_gb300 import build
+    build.build()
+    return torch
+
+
+def make_head(torch_cuda, d, dd, *, max_B, max_gamma, flags=0, grid=0, timeout_us=0):
+    from speculative_decoding_serial_gb300 import whead as wh
+    return wh.Head(dd["W"], dd["E"], kind=d["kind"], A=dd["A"], c=dd["c"], max_B=max_B, max_gamma=max_gamma,
+                   flags=flags | wh.FLAG_LOGITS_F32, grid=grid, timeout_us=timeout_us)
+
+
+SMALL = [
+    # kind, V, r, B, gamma, T, grid
+    (O.MARKOV, 12 * 16, 64, 1, 3, 0.0, 0),
+    (O.MARKOV, 1000, 64, 1, 4, 0.0, 0),
+    (O.MARKOV, 4097, 128, 3, 5, 0.0, 0),
+    (O.MARKOV, 5003, 192, 2, 4, 0.0, 7),
+    (O.MARKOV, 20011, 256, 1, 6, 0.0, 0),
+    (O.MARKOV, 20011, 256, 8, 3, 0.0, 0),
+    (O.MARKOV, 7777, 256, 9, 3, 0.0, 0),
+    (O.MARKOV, 7777, 128, 16, 2, 0.0, 0),
+    (O.MARKOV, 3001, 64, 4, 5, 1.0, 0),
+    (O.MARKOV, 9000, 256, 2, 4, 0.7, 0),
+    (O.RECURRENT, 3001, 64, 1, 5, 0.0, 0),
+    (O.RECURRENT, 9000, 256, 2, 4, 0.0, 0),
+    (O.RECURRENT, 4000, 128, 3, 4, 1.0, 0),
+    # many CTAs with few groups each: every CTA takes part in the exchange
+    (O.MARKOV, 30000, 64, 2, 4, 0.0, 152),
+]
+
+
+@pytest.mark.parametrize("kind,V,r,B,gamma,T,grid", SMALL)
+def test_small_parity(torch_cuda, kind, V, r, B, gamma, T, grid):
+    d = I.make_inputs(kind, V, r, B, gamma, seed=V + r + B)
+    dd = to_device(d, "cuda")
+    head = make_head(torch_cuda, d, dd, max_B=B, max_gamma=gamma, grid=grid)
+    near = []
+    check_walk(head, d, dd, T=T, seed=1234, report=near)
+    if near:
+        print("near-tie steps:", near)
+    head.close()
+
+
+def test_bf16_logits_single_rounding(torch_cuda):
+    from speculative_decoding_serial_gb300 import whead as wh
+    torch = torch_cuda
+    d = I.make_inputs(O.MARKOV, 6000, 128, 2, 3, seed=5)
+    dd = to_device(d, "cuda")
+    head = wh.Head(dd["W"], dd["E"], kind=O.MARKOV, max_B=2, max_gamma=3)
+    lg = torch.empty((2, 3, 6000), dtype=torch.bfloat16, device="cuda")
+    tok = head.walk(dd["base"], dd["s0"], out_logits=lg)
+    assert head.status() == 0
+    ref = O.walk(O.MARKOV, d["W"], d["E"], d["base"], d["s0"], want_z=True, want_logits=True)
+    assert (tok.cpu().numpy() == ref["tokens"]).all() or (ref["gap"] <= GAP).any()
+    got = bf16_to_f32(lg.view(torch.int16).cpu().numpy().view(np.uint16))
+    want = bf16_to_f32(ref["logits"])
+    diff = got != want
+    # a mismatch is allowed only one bf16 ulp away and where z sits within float noise of a midpoint
+    if diff.any():
+        ulp = np.abs(np.nextafter(want, np.inf) - want) * 256  # bf16 ulp = 2^16 fp32 ulps; coarse bound
+        assert np.all(np.abs(got[diff] - want[diff]) <= ulp[diff])
+        assert diff.mean() < 1e-4
+    head.close()
+
+
+def test_resume_from_any_step_bit_exact(torch_cuda):
+    torch = torch_cuda
+    d = I.make_inputs(O.RECURRENT, 8000, 128, 2, 6, seed=9)
+    dd = to_device(d, "cuda")
+    head = make_head(torch_cuda, d, dd, max_B=2, max_gamma=6)
+    full = run_gpu(head, dd, 2, 6, 1.0, 77)
+    for t0 in range(1, 6):
+        part = run_gpu(head, dd, 2, 6 - t0, 1.0, 77, t0=t0, base=dd["base"][:, t0:].contiguous(),
+                       s0=torch.from_numpy(full["state"][:, t0 - 1].copy()).cuda())
+        np.testing.assert_array_equal(part["tokens"], full["tokens"][:, t0:])
+        np.testing.assert_array_equal(part["z"], full["z"][:, t0:])
+        np.testing.assert_array_equal(part["state"], full["state"][:, t0:])
+    head.close()
+
+
+def test_deterministic(torch_cuda):
+    d = I.make_inputs(O.MARKOV, 50000, 256, 4, 5, seed=3)
+    dd = to_device(d, "cuda")
+    head = make_head(torch_cuda, d, dd, max_B=4, max_gamma=5)
+    a = run_gpu(head, dd, 4, 5, 1.0, 5)
+    b = run_gpu(head, dd, 4, 5, 1.0, 5)
+    for k in ("tokens", "z", "state"):
+        np.testing.assert_array_equal(a[k], b[k])
+    head.close()
+
+
+def test_host_entry_point_matches_device(torch_cuda):
+    from speculative_decoding_serial_gb300 import whead as wh
+    torch = torch_cuda
+    d = I.make_inputs(O.MARKOV, 10000, 128, 2, 4, seed=21)
+    dd = to_device(d, "cuda")
+    head = wh.Head(dd["W"], dd["E"], kind=O.MARKOV, max_B=2, max_gamma=4)
+    dev_tok = head.walk(dd["base"], dd["s0"], T=1.0, seed=8).cpu()
+    base_h = torch.from_numpy(d["base"]).pin_memory()
+    s0_h = torch.from_numpy(d["s0"]).pin_memory()
+    host_tok = head.walk_host(base_h, s0_h, T=1.0, seed=8)
+    assert torch.equal(dev_tok, host_tok)
+    head.close()
+
+
+def test_wait_limit_reports_timeout_and_context_survives(torch_cuda):
+    """CTA 0 skips its first arrival (a host flag); every other CTA's bounded wait must run out."""
+    from speculative_decoding_serial_gb300 import whead as wh
+    d = I.make_inputs(O.MARKOV, 40000, 128, 1, 3, seed=2)
+    dd = to_device(d, "cuda")
+    bad = wh.Head(dd["W"], dd["E"], kind=O.MARKOV, max_B=1, max_gamma=3, flags=wh.FLAG_FAULT_SKIP_ARRIVAL,
+                  timeout_us=20000)
+    bad.walk(dd["base"], dd["s0"])
+    assert bad.status() == wh.ERR_TIMEOUT
+    assert bad.status() == 0  # cleared after reading
+    bad.close()
+    good = wh.Head(dd["W"], dd["E"], kind=O.MARKOV, max_B=1, max_gamma=3)
+    tok = good.walk(dd["base"], dd["s0"]).cpu().numpy()
+    assert good.status() == 0
+    ref = O.walk(O.MARKOV, d["W"], d["E"], d["base"], d["s0"])
+    assert ((tok == ref["tokens"]) | (ref["gap"] <= GAP)).all()
+    good.close()
+
+
+def test_invalid_arguments(torch_cuda):
+    from speculative_decoding_serial_gb300 import whead as wh
+    torch = torch_cuda
+    d = I.make_inputs(O.MARKOV, 1000, 64, 1, 2, seed=1)
+    dd = to_device(d, "cuda")
+    head = wh.Head(dd["W"], dd["E"], kind=O.MARKOV, max_B=1, max_gamma=2)
+    big = torch.zeros((2, 2, 1000), dtype=torch.float32, device="cuda")
+    with pytest.raises(wh.WheadError) as e:
+        head.walk(big, torch.zeros((2, 64), device="cuda"))
+    assert e.value.code == wh.ERR_INVALID_ARG
+    with pytest.raises(wh.WheadError):
+        head.walk(dd["base"], dd["s0"], T=-1.0)
+    head.close()
+    Wbad = torch.zeros((100, 96), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(wh.WheadError) as e:
+        wh.Head(Wbad, Wbad, kind=O.MARKOV)
+    assert e.value.code == wh.ERR_UNSUPPORTED
+
+
+# --- the workloads of the pages at full size -------------------------------------------------------
+@pytest.mark.parametrize("name", ["markov_v4096_r64_b1_g4", "markov_v151936_r256_b1_g16",
+                                  "recurrent_v151936_r256_b1_g15"])
+def test_workload_parity(torch_cuda, name):
+    w = I.WORKLOADS[name]
+    d = I.workload_inputs(name)
+    dd = to_device(d, "cuda")
+    head = make_head(torch_cuda, d, dd, max_B=w["B"], max_gamma=w["gamma"])
+    plan = head.plan(w["B"])
+    print(name, plan)
+    near = []
+    check_walk(head, d, dd, T=w["T"], seed=0, report=near)
+    print("near-tie steps:", near)
+    head.close()
+
+
+@pytest.mark.parametrize("B,T", [(1, 1.0), (2, 0.0), (4, 1.0), (8, 0.0)])
+def test_sweep_points_full_vocab(torch_cuda, B, T):
+    """Points of the batch x temperature sweep at V = 151,936, r = 256 (gamma 7)."""
+    d = I.make_inputs(O.MARKOV, 151936, 256, B, 7, seed=0)
+    dd = to_device(d, "cuda")
+    head = make_head(torch_cuda, d, dd, max_B=B, max_gamma=7)
+    assert head.plan(B)["stream_groups"] == 0
+    check_walk(head, d, dd, T=T, seed=11)
+    head.close()
