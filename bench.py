@@ -1,0 +1,344 @@
+"""Benchmark of the walk-resident serial draft head.
+
+Metric: microseconds per gamma = 16 draft walk (B = 1, V = 151,936, r = 256, greedy Markov head) and the
+fraction of the on-chip-bandwidth roofline. One "step" of this benchmark is one whole walk (one kernel
+launch) over synthetic inputs that are resident in HBM; the L2 cache is flushed (256 MB write) before
+every timed walk, outside the timed interval. Per-walk times come from CUDA events on the walk's stream.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+With N > 1 (torchrun) every rank runs an independent replica (no data-path collective); the job's value
+is the slowest rank's timed total divided by all walks of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "us per gamma=16 draft walk (B=1, V=152k, greedy) & % of on-chip-BW roofline"
+DEFAULT_WORKLOAD = "markov_v151936_r256_b1_g16"
+
+# Per-SM on-chip figures used by the roofline (bytes per SM clock). Shared memory: 32 banks x 4 B.
+# Tensor memory read by tcgen05.ld: measured on GB300 with an in-bounds probe (32x32b.x64, 512 threads).
+SMEM_B_PER_CLK = 128.0
+TMEM_B_PER_CLK = 428.0
+TMEM_BYTES = 128 * 512 * 4
+# Registers this kernel family can dedicate to W: one 16-row group per warp, 12 warps.
+RF_W_BYTES_CAP = 12 * 16 * 512
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d.get("hbm_gbs", 6800.0)), "measured"
+    return 6800.0, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                                          "-i", self.gpu_id, "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.path) as f:
+                for line in f:
+                    parts = [x.strip() for x in line.split(",")]
+                    if len(parts) >= 9 and parts[1].replace(".", "").isdigit():
+                        rows.append(parts)
+        except Exception:
+            pass
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        smax = max(float(r[2]) for r in rows)
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": reasons, "samples": len(rows)}
+
+
+def gpu_selector(torch, dev):
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        bus = getattr(p, "pci_bus_id", None)
+        dom = getattr(p, "pci_domain_id", None)
+        devid = getattr(p, "pci_device_id", None)
+        if bus is not None and dom is not None and devid is not None:
+            return f"{dom:08x}:{bus:02x}:{devid:02x}.0"
+    except Exception:
+        pass
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+    if vis:
+        return vis.split(",")[dev]
+    return str(dev)
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            import torch
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def oracle_walk_time(d, gamma_sample, repeats):
+    """Wall time of the oracle on `repeats` samples of `gamma_sample` steps of the workload (1 thread)."""
+    from oracle import oracle as O
+    base = d["base"][:, :gamma_sample].copy()
+    t = time.perf_counter()
+    for _ in range(repeats):
+        O.walk(d["kind"], d["W"], d["E"], base, d["s0"], A=d["A"], c=d["c"], T=d["T"], want_gap=False)
+    return (time.perf_counter() - t) / repeats
+
+
+def reference_arm(args, world, rank):
+    """The oracle, as it stands, on this host's cores: each step is one walk step of the workload."""
+    if rank != 0:
+        return
+    import whead_inputs as I
+    from oracle import oracle as O
+    w = I.WORKLOADS[args.workload]
+    d = I.workload_inputs(args.workload)
+    base1 = d["base"][:, :1].copy()
+    for _ in range(args.warmup):
+        O.walk(d["kind"], d["W"], d["E"], base1, d["s0"], A=d["A"], c=d["c"], T=d["T"], want_gap=False)
+    t = time.perf_counter()
+    for k in range(args.steps):
+        s0 = d["s0"]
+        O.walk(d["kind"], d["W"], d["E"], d["base"][:, k % w["gamma"]:k % w["gamma"] + 1].copy(), s0, A=d["A"],
+               c=d["c"], T=d["T"], t0=k % w["gamma"], want_gap=False)
+    per_step = (time.perf_counter() - t) / args.steps
+    value = per_step * w["gamma"] * 1e6
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "us/walk", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": args.workload, **{k: w[k] for k in ("V", "r", "B", "gamma", "T")}},
+        "cpu_baseline": {"value": value, "unit": "us/walk", "cores": 1, "kind": "oracle",
+                         "sample": f"{args.steps} single walk steps of the workload (x{w['gamma']} for a walk)"},
+        "e2e": {"value": value, "unit": "us/walk", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def ours(args, world, rank, local):
+    import numpy as np
+    import torch
+
+    import whead_inputs as I
+    from speculative_decoding_serial_gb300 import build
+    from speculative_decoding_serial_gb300 import whead as wh
+
+    if rank == 0 or not build.needs_build():
+        build.build()
+    barrier(world)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = I.WORKLOADS[args.workload]
+    d = I.workload_inputs(args.workload)
+    B, gamma, V, r = w["B"], w["gamma"], w["V"], w["r"]
+    W = torch.from_numpy(d["W"].view(np.int16)).view(torch.bfloat16).to(dev)
+    E = torch.from_numpy(d["E"].view(np.int16)).view(torch.bfloat16).to(dev)
+    base = torch.from_numpy(d["base"]).to(dev)
+    s0 = torch.from_numpy(d["s0"]).to(dev)
+    A = None if d["A"] is None else torch.from_numpy(d["A"]).to(dev)
+    c = None if d["c"] is None else torch.from_numpy(d["c"]).to(dev)
+    stream = torch.cuda.current_stream(dev)
+    head = wh.Head(W, E, kind=w["kind"], A=A, c=c, max_B=B, max_gamma=gamma, stream=stream)
+    plan = head.plan(B)
+    tok = torch.empty((B, gamma), dtype=torch.int32, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def timed_walks(n, g, record=True):
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        bg = base[:, :g].contiguous() if g != gamma else base
+        tk = tok[:, :g].contiguous() if g != gamma else tok
+        for k in range(n):
+            flush.zero_()
+            ev[k][0].record(stream)
+            head.walk(bg, s0, T=w["T"], seed=0, out_tokens=tk)
+            ev[k][1].record(stream)
+        torch.cuda.synchronize(dev)
+        return [a.elapsed_time(b) for a, b in ev]
+
+    timed_walks(args.warmup, gamma)
+    assert head.status() == 0
+
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(gpu_selector(torch, local)) as clk:
+        times_ms = timed_walks(args.steps, gamma)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    st = head.status()
+    if st != 0:
+        raise RuntimeError(f"device status {st} during the timed walks")
+    total_ms = max_over_ranks(sum(times_ms), world)
+    us_per_walk = total_ms * 1e3 / (args.steps * world)
+    clocks = clk.summary()
+
+    # per-step cost: least-squares slope over gamma in {1, 7, 16}; intercept = entry cost
+    fit_g, fit_t = [], []
+    for g in (1, 7, 16):
+        if g > gamma:
+            continue
+        ts = timed_walks(max(20, min(200, args.steps)), g)
+        fit_g.append(g)
+        fit_t.append(statistics.median(ts) * 1e3)
+    slope = intercept = None
+    if len(fit_g) >= 2:
+        gm, tm = sum(fit_g) / len(fit_g), sum(fit_t) / len(fit_t)
+        slope = sum((a - gm) * (b - tm) for a, b in zip(fit_g, fit_t)) / sum((a - gm) ** 2 for a in fit_g)
+        intercept = tm - slope * gm
+
+    # roofline (on-chip operand bandwidth for the steps, HBM for the one-time shard load)
+    hbm_gbs, peak_kind = load_peaks()
+    sm = plan["sm_count"]
+    wbytes = V * r * 2
+    w_per_sm = plan["groups_per_cta"] * 16 * r * 2
+    smem_min = max(0, w_per_sm - TMEM_BYTES - RF_W_BYTES_CAP)
+    tmem_used = min(TMEM_BYTES, w_per_sm)
+    t_star_clk = max(smem_min / SMEM_B_PER_CLK, tmem_used / TMEM_B_PER_CLK)
+    mhz = clocks["sm_mhz"] or 1447.0
+    t_star_us = t_star_clk / mhz
+    t_entry_us = wbytes / (hbm_gbs * 1e3)
+    t_roof_us = t_entry_us + gamma * t_star_us
+    alg_bytes = wbytes + gamma * wbytes + B * gamma * V * 4 + gamma * B * r * 2
+    achieved = alg_bytes / (us_per_walk * 1e3)
+    peak = alg_bytes / (t_roof_us * 1e3)
+
+    # end to end through the host-buffer entry point: pinned inputs copied in, tokens copied out
+    base_h = torch.from_numpy(d["base"]).pin_memory()
+    s0_h = torch.from_numpy(d["s0"]).pin_memory()
+    tok_h = torch.empty((B, gamma), dtype=torch.int32).pin_memory()
+    for _ in range(5):
+        head.walk_host(base_h, s0_h, T=w["T"], out_tokens=tok_h)
+    n_e2e = max(20, min(200, args.steps))
+    e2e = []
+    for _ in range(n_e2e):
+        flush.zero_()
+        torch.cuda.synchronize(dev)
+        t = time.perf_counter()
+        head.walk_host(base_h, s0_h, T=w["T"], out_tokens=tok_h)
+        e2e.append(time.perf_counter() - t)
+    e2e_us = max_over_ranks(statistics.mean(e2e) * 1e6, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        one = oracle_walk_time(d, gamma, 1)
+        reps = max(1, min(50, int(math.ceil(args.cpu_seconds / max(one, 1e-3)))))
+        per = oracle_walk_time(d, gamma, reps)
+        cpu = {"value": per * 1e6, "unit": "us/walk", "cores": 1, "kind": "oracle",
+               "sample": f"{reps} full walks of {args.workload} (single thread)"}
+
+    head.close()
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": us_per_walk, "unit": "us/walk", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": us_per_walk / 1e3, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": args.workload, "V": V, "r": r, "B": B, "gamma": gamma, "T": w["T"],
+                   "l2": "flushed (256 MB write) before every timed walk", "placement": plan},
+        "roofline": {"bound": "onchip", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": t_roof_us / us_per_walk, "traffic": None,
+                     "t_roof_us": t_roof_us, "t_entry_us": t_entry_us, "t_star_clk_per_step": t_star_clk,
+                     "hbm_peak_gbs": hbm_gbs, "hbm_peak_kind": peak_kind, "clock_mhz": mhz},
+        "per_step": {"slope_us": slope, "intercept_us": intercept, "gammas": fit_g, "median_us": fit_t,
+                     "t_star_us": t_star_us,
+                     "frac_of_onchip_roofline": (t_star_us / slope) if slope else None},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_us, "unit": "us/walk", "h2d_bytes_per_step": B * gamma * V * 4 + B * r * 4,
+                "d2h_bytes_per_step": B * gamma * 4},
+        "clocks": clocks,
+        "gpu_launches": args.steps,
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        reference_arm(args, world, rank)
+    else:
+        ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
