@@ -130,6 +130,36 @@ const char* whead_strerror(int code);
 /* Frees the handle and its scratch. Waits for the handle's stream first. */
 int whead_destroy(whead_t* h);
 
+/*
+ * Walk without any device allocation. The paper has no counterpart: this entry point exists for callers
+ * that must not call cudaMalloc, such as serving engines that reserve all GPU memory up front in their own
+ * pool (an extra cudaMalloc may fail or bypass the pool's accounting) and latency-critical loops where a
+ * cudaMalloc/cudaFree would synchronize the device. It runs the same walk as whead_walk with no handle:
+ * the placement and the TMA descriptor of W are built on the host for every call, and the walk's scratch
+ * (exchange slots, arrival counter, A h slices, status word) lives in one file-scope device array of
+ * WHEAD_NOALLOC_SCRATCH_BYTES that every GPU loading this library keeps until the process exits.
+ *
+ * Arguments: W, E and params as for whead_create (params->max_B, max_gamma and grid are ignored: the call
+ * plans for its own B and gamma; params->stream is the stream used); base, u0, B, gamma, T, seed,
+ * out_tokens and out_logits as for whead_walk. out_status: NULL, or a device int32 that receives the
+ * call's device status (0, or WHEAD_ERR_TIMEOUT / WHEAD_ERR_INTERNAL) once the stream reaches the end of
+ * the walk. All pointers are device pointers owned by the caller.
+ *
+ * Errors: WHEAD_ERR_INVALID_ARG / WHEAD_ERR_UNSUPPORTED as whead_create and whead_walk; a call whose
+ * scratch would exceed WHEAD_NOALLOC_SCRATCH_BYTES is rejected with WHEAD_ERR_UNSUPPORTED (it cannot
+ * happen within the documented limits B <= 16, gamma <= 64, r <= 256).
+ *
+ * Every call shares the one array and clears what must start at zero (slots, counter, status) with
+ * cudaMemsetAsync on the call's stream. Calls whose walks overlap on the GPU (different streams, or several
+ * host threads) race on the array and give wrong results: serialize them. The first call on a device
+ * looks up the array's device address (cudaGetSymbolAddress) and the device's limits; make that first call
+ * before any stream capture.
+ */
+#define WHEAD_NOALLOC_SCRATCH_BYTES (64 * 1024)
+int whead_walk_noalloc(const void* W, const void* E, const whead_params* params, const float* base,
+                       const float* u0, int32_t B, int32_t gamma, float T, uint64_t seed, int32_t* out_tokens,
+                       void* out_logits, int32_t* out_status);
+
 #ifdef __cplusplus
 }
 #endif

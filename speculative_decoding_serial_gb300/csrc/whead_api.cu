@@ -421,3 +421,166 @@ int whead_destroy(whead_t* h) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------------------------------
+// Entry point without allocation: the scratch lives in one file-scope device array.
+// ------------------------------------------------------------------------------------------------
+namespace {
+
+// Layout of the array: [slots 8 KB | counter 128 B | status 128 B] (cleared every call) then
+// [slots of the other parity 8 KB | its counter 128 B] (cleared by the kernel) then [A h slices].
+constexpr size_t kNaSlots = (size_t)kMaxGamma * kMaxB * 8;
+constexpr size_t kNaZeroBytes = kNaSlots + 256;
+constexpr size_t kNaOtherOff = kNaZeroBytes;
+constexpr size_t kNaAhOff = kNaOtherOff + kNaSlots + 128;
+static_assert(kNaAhOff + 2 * (size_t)kMaxB * 256 * 4 <= WHEAD_NOALLOC_SCRATCH_BYTES, "scratch array too small");
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[WHEAD_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kNaMaxDevices = 64;
+struct NaDevice {
+  void* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+  int sm_count = 0, smem_optin = 0, coop = 0;
+  bool ready = false;
+};
+NaDevice g_na_devices[kNaMaxDevices];
+
+// Once per device, with that device current: the array's device address and the device limits.
+int noalloc_setup(int dev, NaDevice** out) {
+  if (dev < 0 || dev >= kNaMaxDevices) return WHEAD_ERR_UNSUPPORTED;
+  NaDevice& d = g_na_devices[dev];
+  if (!d.ready) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+      (void)cudaGetLastError();
+      return WHEAD_ERR_CUDA;
+    }
+    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&d.coop, cudaDevAttrCooperativeLaunch, dev) != cudaSuccess)
+      return WHEAD_ERR_CUDA;
+    d.scratch = p;
+    d.ready = true;
+  }
+  *out = &d;
+  return WHEAD_OK;
+}
+
+template <int KB, int NH>
+int noalloc_launch_t(const CUtensorMap& tmap, cudaStream_t stream, int smem_optin, const Plan& pl, const WalkArgs& a) {
+  auto fn = walk_kernel<KB, NH>;
+  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin) != cudaSuccess)
+    return WHEAD_ERR_CUDA;
+  void* args[] = {(void*)&tmap, (void*)&a};
+  cudaError_t e = cudaLaunchCooperativeKernel((const void*)fn, dim3(pl.G), dim3(kThreads), args, (size_t)pl.smem_bytes,
+                                              stream);
+  if (e == cudaErrorCooperativeLaunchTooLarge) {
+    (void)cudaGetLastError();
+    return WHEAD_ERR_NO_COOP;
+  }
+  if (e != cudaSuccess) {
+    (void)cudaGetLastError();
+    return WHEAD_ERR_CUDA;
+  }
+  return WHEAD_OK;
+}
+
+int noalloc_launch(int r, int NH, const CUtensorMap& tmap, cudaStream_t stream, int smem_optin, const Plan& pl,
+                   const WalkArgs& a) {
+  switch (kb_of(r) * 2 + (NH - 1)) {
+    case 2: return noalloc_launch_t<1, 1>(tmap, stream, smem_optin, pl, a);
+    case 3: return noalloc_launch_t<1, 2>(tmap, stream, smem_optin, pl, a);
+    case 4: return noalloc_launch_t<2, 1>(tmap, stream, smem_optin, pl, a);
+    case 5: return noalloc_launch_t<2, 2>(tmap, stream, smem_optin, pl, a);
+    case 6: return noalloc_launch_t<3, 1>(tmap, stream, smem_optin, pl, a);
+    case 7: return noalloc_launch_t<3, 2>(tmap, stream, smem_optin, pl, a);
+    case 8: return noalloc_launch_t<4, 1>(tmap, stream, smem_optin, pl, a);
+    case 9: return noalloc_launch_t<4, 2>(tmap, stream, smem_optin, pl, a);
+    default: return WHEAD_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace
+
+extern "C" int whead_walk_noalloc(const void* W, const void* E, const whead_params* params, const float* base,
+                                  const float* u0, int32_t B, int32_t gamma, float T, uint64_t seed,
+                                  int32_t* out_tokens, void* out_logits, int32_t* out_status) {
+  if (!W || !E || !params || !base || !u0 || !out_tokens) return WHEAD_ERR_INVALID_ARG;
+  const whead_params& p = *params;
+  if (p.kind != WHEAD_MARKOV && p.kind != WHEAD_RECURRENT) return WHEAD_ERR_INVALID_ARG;
+  if (p.V < 1 || B < 1 || gamma < 1) return WHEAD_ERR_INVALID_ARG;
+  if (B > kMaxB || gamma > kMaxGamma) return WHEAD_ERR_UNSUPPORTED;  // beyond the scratch array's sizes
+  if (p.V >= (int64_t)1 << 24) return WHEAD_ERR_UNSUPPORTED;
+  if (p.r != 64 && p.r != 128 && p.r != 192 && p.r != 256) return WHEAD_ERR_UNSUPPORTED;
+  if (p.kind == WHEAD_RECURRENT && !p.A) return WHEAD_ERR_UNSUPPORTED;
+  if (!(T >= 0.0f) || T > 3.0e38f) return WHEAD_ERR_INVALID_ARG;
+  if (!aligned16(W) || !aligned16(E) || !aligned16(u0)) return WHEAD_ERR_INVALID_ARG;
+  const size_t need = kNaAhOff + 2 * (size_t)kMaxB * p.r * 4;
+  if (need > WHEAD_NOALLOC_SCRATCH_BYTES) return WHEAD_ERR_UNSUPPORTED;
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return WHEAD_ERR_CUDA;
+  NaDevice* nd = nullptr;
+  int rc = noalloc_setup(dev, &nd);
+  if (rc != WHEAD_OK) return rc;
+  if (!nd->coop) return WHEAD_ERR_NO_COOP;
+
+  const int NH = B <= 8 ? 1 : 2;
+  const Plan pl = make_plan(p.V, p.r, p.kind, B, NH, nd->sm_count, nd->smem_optin, 0);
+  if (!pl.ok) return WHEAD_ERR_UNSUPPORTED;
+
+  auto encode = get_encode();
+  if (!encode) return WHEAD_ERR_CUDA;
+  CUtensorMap tmap;
+  cuuint64_t gdim[2] = {(cuuint64_t)p.r, (cuuint64_t)p.V};
+  cuuint64_t gstride[1] = {(cuuint64_t)p.r * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)kGroupRows};
+  cuuint32_t estride[2] = {1, 1};
+  if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W), gdim, gstride, box, estride,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return WHEAD_ERR_CUDA;
+
+  cudaStream_t stream = static_cast<cudaStream_t>(p.stream);
+  uint8_t* sc = static_cast<uint8_t*>(nd->scratch);
+  if (cudaMemsetAsync(sc, 0, kNaZeroBytes, stream) != cudaSuccess) return WHEAD_ERR_CUDA;
+  if (out_status && cudaMemsetAsync(out_status, 0, sizeof(int32_t), stream) != cudaSuccess) return WHEAD_ERR_CUDA;
+
+  WalkArgs a;
+  std::memset(&a, 0, sizeof(a));
+  a.W = static_cast<const uint16_t*>(W);
+  a.E = static_cast<const uint16_t*>(E);
+  a.A = p.A;
+  a.c = p.c;
+  a.base = base;
+  a.s0 = u0;
+  a.tokens = out_tokens;
+  a.logits = out_logits;
+  a.state = nullptr;
+  a.slots = reinterpret_cast<unsigned long long*>(sc);
+  a.cnt = reinterpret_cast<unsigned int*>(sc + kNaSlots);
+  a.slots_reset = reinterpret_cast<unsigned long long*>(sc + kNaOtherOff);
+  a.cnt_reset = reinterpret_cast<unsigned int*>(sc + kNaOtherOff + kNaSlots);
+  a.ah = reinterpret_cast<float*>(sc + kNaAhOff);
+  a.status = out_status ? reinterpret_cast<int*>(out_status) : reinterpret_cast<int*>(sc + kNaSlots + 128);
+  a.V = p.V;
+  a.t0 = 0;
+  a.seed = seed;
+  a.timeout_ns = (uint64_t)(p.timeout_us ? p.timeout_us : 1000000u) * 1000ull;
+  a.T = T;
+  a.r = p.r;
+  a.B = B;
+  a.gamma = gamma;
+  a.kind = p.kind;
+  a.flags = p.flags;
+  a.ng = pl.ng;
+  a.n_smem = pl.n_smem;
+  a.n_tmem = pl.n_tmem;
+  a.n_rf = pl.n_rf;
+  a.tmem_cols = pl.tmem_cols;
+  a.smem_w_bytes = pl.smem_w_bytes;
+  a.ra = pl.ra;
+  std::memcpy(a.wl_count, pl.wl_count, sizeof(a.wl_count));
+  std::memcpy(a.wl, pl.wl, sizeof(a.wl));
+  return noalloc_launch(p.r, NH, tmap, stream, nd->smem_optin, pl, a);
+}

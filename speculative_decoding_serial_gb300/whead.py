@@ -28,7 +28,7 @@ ERR_INTERNAL = -6
 
 # Every symbol include/whead.h declares.
 EXPORTS = ("whead_create", "whead_walk", "whead_walk_ex", "whead_walk_host", "whead_status",
-           "whead_plan_info", "whead_strerror", "whead_destroy")
+           "whead_plan_info", "whead_strerror", "whead_destroy", "whead_walk_noalloc")
 
 
 class WheadParams(ctypes.Structure):
@@ -77,8 +77,9 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     L.whead_strerror.argtypes = [ctypes.c_int]
     L.whead_strerror.restype = ctypes.c_char_p
     L.whead_destroy.argtypes = [vp]
+    L.whead_walk_noalloc.argtypes = [vp, vp, ctypes.POINTER(WheadParams), vp, vp, i32, i32, f32, u64, vp, vp, vp]
     for name in ("whead_create", "whead_walk", "whead_walk_ex", "whead_walk_host", "whead_status",
-                 "whead_plan_info", "whead_destroy"):
+                 "whead_plan_info", "whead_destroy", "whead_walk_noalloc"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -174,3 +175,24 @@ class Head:
             self.close()
         except Exception:
             pass
+
+
+def walk_noalloc(W, E, base, u0, *, kind=MARKOV, A=None, c=None, T=0.0, seed=0, flags=0, timeout_us=0,
+                 out_tokens, out_logits=None, out_status=None, stream=None):
+    """The allocation-free walk (whead_walk_noalloc): every buffer, outputs included, comes from the caller.
+
+    For callers that must not allocate device memory (an engine that owns all GPU memory in its own pool,
+    or a loop that cannot afford the device synchronization of cudaMalloc). The library's scratch for this
+    call is a fixed device array shared by all calls, so walks issued through this function must not
+    overlap on the GPU. The first call on a device should come before any stream capture.
+    """
+    import torch
+    B, gamma, V = base.shape
+    r = int(W.shape[1])
+    s = torch.cuda.current_stream() if stream is None else stream
+    p = WheadParams(kind=int(kind), r=r, V=int(V), A=_ptr(A), c=_ptr(c), max_B=int(B), max_gamma=int(gamma),
+                    stream=ctypes.c_void_p(s.cuda_stream), flags=int(flags), grid=0, timeout_us=int(timeout_us))
+    _check(load().whead_walk_noalloc(_ptr(W), _ptr(E), ctypes.byref(p), _ptr(base), _ptr(u0), int(B), int(gamma),
+                                     float(T), int(seed) & (2**64 - 1), _ptr(out_tokens), _ptr(out_logits),
+                                     _ptr(out_status)), "whead_walk_noalloc")
+    return out_tokens
