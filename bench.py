@@ -154,6 +154,42 @@ def oracle_walk_time(d, gamma_sample, repeats):
     return (time.perf_counter() - t) / repeats
 
 
+def trace_phases(torch, head, base, s0, tok, w, plan, flush, stream, dev, walks=20):
+    """Per-step phase durations from the kernel's phase stamps (median over walks, steps 1.., and CTAs)."""
+    gamma, G = w["gamma"], plan["grid"]
+    S = 4 + 8 * gamma
+    buf = torch.zeros((G, S), dtype=torch.int64, device=dev)
+    head.set_trace(buf)
+    rows = []
+    for _ in range(walks):
+        flush.zero_()
+        head.walk(base, s0, T=w["T"], seed=0, out_tokens=tok)
+        torch.cuda.synchronize(dev)
+        rows.append(buf.cpu().numpy().copy())
+    head.set_trace(None)
+    import numpy as np
+    a = np.stack(rows).astype(np.int64)            # walks x G x S
+    half = S // 2
+    clk, ns = a[:, :, :half], a[:, :, half:]
+    st = lambda t, i: 2 + 4 * t + i
+    proj, exch, adv, skew, step_ns = [], [], [], [], []
+    for t in range(1, gamma):
+        proj.append(clk[:, :, st(t, 1)] - clk[:, :, st(t, 0)])
+        exch.append(clk[:, :, st(t, 2)] - clk[:, :, st(t, 1)])
+        adv.append(clk[:, :, st(t, 3)] - clk[:, :, st(t, 2)])
+        done = ns[:, :, st(t, 1)]
+        skew.append(done.max(axis=1) - done.min(axis=1))
+        step_ns.append(ns[:, :, st(t, 3)].max(axis=1) - ns[:, :, st(t - 1, 3)].max(axis=1))
+    med = lambda x: float(np.median(np.concatenate([np.ravel(v) for v in x]))) if x else None
+    p90 = lambda x: float(np.percentile(np.concatenate([np.ravel(v) for v in x]), 90)) if x else None
+    entry_ns = ns[:, :, 1] - ns[:, :, 0]
+    return {"walks": walks, "proj_select_clk": med(proj), "proj_select_clk_p90": p90(proj),
+            "exchange_clk": med(exch), "advance_clk": med(adv), "arrival_skew_ns": med(skew),
+            "step_ns": med(step_ns), "entry_ns_median": float(np.median(entry_ns)),
+            "entry_ns_max": float(np.median(entry_ns.max(axis=1))),
+            "exchange_share": (med(exch) / (med(proj) + med(exch) + med(adv))) if proj else None}
+
+
 def reference_arm(args, world, rank):
     """The oracle, as it stands, on this host's cores: each step is one walk step of the workload."""
     if rank != 0:
@@ -270,6 +306,8 @@ def ours(args, world, rank, local):
     achieved = alg_bytes / (us_per_walk * 1e3)
     peak = alg_bytes / (t_roof_us * 1e3)
 
+    phases = trace_phases(torch, head, base, s0, tok, w, plan, flush, stream, dev)
+
     # end to end through the host-buffer entry point: pinned inputs copied in, tokens copied out
     base_h = torch.from_numpy(d["base"]).pin_memory()
     s0_h = torch.from_numpy(d["s0"]).pin_memory()
@@ -314,6 +352,7 @@ def ours(args, world, rank, local):
         "e2e": {"value": e2e_us, "unit": "us/walk", "h2d_bytes_per_step": B * gamma * V * 4 + B * r * 4,
                 "d2h_bytes_per_step": B * gamma * 4},
         "clocks": clocks,
+        "phases": phases,
         "gpu_launches": args.steps,
     }
     print(json.dumps(line))

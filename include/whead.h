@@ -118,6 +118,16 @@ int whead_walk_ex(whead_t* h, const float* base, const float* s0, int32_t B, int
 int whead_walk_host(whead_t* h, const float* base_host, const float* u0_host, int32_t B, int32_t gamma,
                     float T, uint64_t seed, int32_t* out_tokens_host, void* out_logits_host);
 
+/*
+ * Profiling aid: phase stamps of every CTA for the following walks on this handle (NULL turns it off).
+ * trace: device buffer of uint64, 8-byte aligned, of at least grid x S x 8 bytes with S = 4 + 8 * gamma
+ * (grid from whead_plan_info); a walk that does not fit writes no stamps. Row c (S words) of CTA c holds
+ * S/2 SM-clock stamps followed by the same S/2 stamps as global-timer nanoseconds: [0] kernel start,
+ * [1] shard loaded, then for step t at 2 + 4t: step start, projection and local selection done, exchange
+ * done (thread 0 saw every CTA's arrival), state advanced.
+ */
+int whead_set_trace(whead_t* h, void* trace, int64_t bytes);
+
 /* Waits for the handle's stream and returns WHEAD_OK or the first device-side error (then clears it). */
 int whead_status(whead_t* h);
 

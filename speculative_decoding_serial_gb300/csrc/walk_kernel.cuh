@@ -67,6 +67,8 @@ struct WalkArgs {
   unsigned int* cnt_reset;
   float* ah;                        // [2][kMaxB][r]: slices of A h exchanged between CTAs
   int* status;
+  unsigned long long* trace;  // optional phase stamps: [grid][trace_stride] (clock64 half, globaltimer half)
+  int32_t trace_stride;
   int64_t V;
   int64_t t0;
   uint64_t seed;
@@ -120,6 +122,18 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
+
+// Phase stamp k of this CTA (thread 0 only): SM clock in the first half of the CTA's row, global
+// nanosecond timer in the second half.
+__device__ __forceinline__ void trace_stamp(const WalkArgs& P, int k) {
+  if (P.trace != nullptr && threadIdx.x == 0) {
+    unsigned long long* row = P.trace + (int64_t)blockIdx.x * P.trace_stride;
+    row[k] = (unsigned long long)clock64();
+    row[P.trace_stride / 2 + k] = globaltimer_ns();
+  }
+}
+constexpr int kTraceStampsPerStep = 4;
+__host__ __device__ constexpr int trace_stride_for(int max_gamma) { return 2 * (2 + kTraceStampsPerStep * max_gamma); }
 
 __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                                uint32_t b0, uint32_t b1) {
@@ -304,6 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* s_A = reinterpret_cast<float*>(smem + L.a);
 
   const uint32_t mbar = smem_u32(s_mbar);
+  trace_stamp(P, 0);
   const int64_t row_base = (int64_t)cta * P.ng * kGroupRows;
 
   // ---------------- set-up ----------------
@@ -405,6 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tmem_fence_before();
   __syncthreads();
   tmem_fence_after();
+  trace_stamp(P, 1);
 
   // ---------------- the walk ----------------
   uint32_t bf[NH][KB][8];
@@ -432,6 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int t = 0; t < gamma; ++t) {
     if (*s_abort) break;
     const uint32_t tau = (uint32_t)(P.t0 + t);
+    trace_stamp(P, 2 + kTraceStampsPerStep * t);
 
     // recurrent: this CTA's slice of A h_t, published with the step's arrival
     if (recurrent && warp == 0) {
@@ -540,6 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (g == 0 && n < B) s_red[warp * kMaxB + n] = k;
       }
     __syncthreads();
+    trace_stamp(P, 2 + kTraceStampsPerStep * t + 1);
 
     // exchange (Fig. 8): CTA winner -> red.max into the step slot, release arrival, bounded acquire poll
     if (warp == 0) {
@@ -567,6 +585,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
         }
+        trace_stamp(P, 2 + kTraceStampsPerStep * t + 2);
         for (int n = 0; n < B; ++n) {
           unsigned long long kn;
           asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(kn) : "l"(slot + n) : "memory");
@@ -624,6 +643,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+    trace_stamp(P, 2 + kTraceStampsPerStep * t + 3);
   }
 
   // ---------------- exit ----------------

@@ -47,6 +47,8 @@ struct whead_s {
   void* scratch_block = nullptr;
   Scratch s{};
   uint32_t parity = 0;
+  unsigned long long* trace = nullptr;
+  int64_t trace_bytes = 0;
   // host-call staging
   float* d_base = nullptr;
   float* d_u0 = nullptr;
@@ -315,6 +317,10 @@ int whead_walk_ex(whead_t* h, const float* base, const float* s0, int32_t B, int
   a.cnt_reset = h->s.cnt + (par ^ 1u) * 32;
   a.ah = h->s.ah;
   a.status = h->s.status;
+  if (h->trace && h->trace_bytes >= (int64_t)pl.G * trace_stride_for(gamma) * 8) {
+    a.trace = h->trace;
+    a.trace_stride = trace_stride_for(gamma);
+  }
   a.V = h->p.V;
   a.t0 = t0;
   a.seed = seed;
@@ -373,6 +379,13 @@ int whead_walk_host(whead_t* h, const float* base_host, const float* u0_host, in
       cudaMemcpyAsync(out_logits_host, h->d_logits, nbase * logit_elem, cudaMemcpyDeviceToHost, h->stream) != cudaSuccess)
     return WHEAD_ERR_CUDA;
   if (cudaStreamSynchronize(h->stream) != cudaSuccess) return WHEAD_ERR_CUDA;
+  return WHEAD_OK;
+}
+
+int whead_set_trace(whead_t* h, void* trace, int64_t bytes) {
+  if (!h || bytes < 0 || (trace && (reinterpret_cast<uintptr_t>(trace) & 7u))) return WHEAD_ERR_INVALID_ARG;
+  h->trace = static_cast<unsigned long long*>(trace);
+  h->trace_bytes = trace ? bytes : 0;
   return WHEAD_OK;
 }
 

@@ -28,7 +28,8 @@ ERR_INTERNAL = -6
 
 # Every symbol include/whead.h declares.
 EXPORTS = ("whead_create", "whead_walk", "whead_walk_ex", "whead_walk_host", "whead_status",
-           "whead_plan_info", "whead_strerror", "whead_destroy", "whead_walk_noalloc")
+           "whead_plan_info", "whead_strerror", "whead_destroy", "whead_walk_noalloc",
+           "whead_set_trace")
 
 
 class WheadParams(ctypes.Structure):
@@ -79,7 +80,8 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     L.whead_destroy.argtypes = [vp]
     L.whead_walk_noalloc.argtypes = [vp, vp, ctypes.POINTER(WheadParams), vp, vp, i32, i32, f32, u64, vp, vp, vp]
     for name in ("whead_create", "whead_walk", "whead_walk_ex", "whead_walk_host", "whead_status",
-                 "whead_plan_info", "whead_destroy", "whead_walk_noalloc"):
+                 "whead_plan_info", "whead_destroy", "whead_walk_noalloc",
+           "whead_set_trace"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -156,6 +158,12 @@ class Head:
         _check(load().whead_walk_host(self._h, _ptr(base), _ptr(u0), B, gamma, float(T), int(seed) & (2**64 - 1),
                                       _ptr(out_tokens), _ptr(out_logits)), "whead_walk_host")
         return out_tokens
+
+    def set_trace(self, buf):
+        """Phase stamps for the following walks (buf: int64 CUDA tensor, or None to turn them off)."""
+        n = 0 if buf is None else buf.numel() * buf.element_size()
+        _check(load().whead_set_trace(self._h, _ptr(buf), n), "whead_set_trace")
+        self._trace = buf
 
     def status(self) -> int:
         return int(load().whead_status(self._h))

@@ -188,3 +188,21 @@ def test_sweep_points_full_vocab(torch_cuda, B, T):
     assert head.plan(B)["stream_groups"] == 0
     check_walk(head, d, dd, T=T, seed=11)
     head.close()
+
+
+def test_phase_trace_stamps_are_ordered(torch_cuda):
+    torch = torch_cuda
+    d = I.make_inputs(O.MARKOV, 60000, 256, 1, 4, seed=4)
+    dd = to_device(d, "cuda")
+    head = make_head(torch_cuda, d, dd, max_B=1, max_gamma=4)
+    G = head.plan(1)["grid"]
+    S = 4 + 8 * 4
+    buf = torch.zeros((G, S), dtype=torch.int64, device="cuda")
+    head.set_trace(buf)
+    run_gpu(head, dd, 1, 4, 0.0, 0)
+    a = buf.cpu().numpy()
+    head.set_trace(None)
+    clk = a[:, :S // 2]
+    assert (clk > 0).all()
+    assert (np.diff(clk, axis=1) >= 0).all()      # stamps of every CTA are in program order
+    head.close()
