@@ -33,6 +33,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 namespace whead {
 
 constexpr int kThreads = 384;
@@ -86,29 +88,33 @@ struct WalkArgs {
   uint32_t tmem_cols;
   int32_t smem_w_bytes;
   int32_t ra;        // recurrent: rows of A per CTA
+  uint32_t rf_warp_mask;  // warps that keep one group in registers (they own no tensor-memory group)
   int32_t wl_count[kWarps];
-  uint8_t wl[kWarps][kMaxWarpGroups];  // CTA-local group indices processed by each warp
+  // work list of each warp: bits 0..7 CTA-local group, bits 8..9 tier, bits 16..25 tensor-memory column
+  uint32_t wl[kWarps][kMaxWarpGroups];
 };
+
+constexpr uint32_t kTierSmem = 0, kTierTmem = 1, kTierRf = 2;
+__host__ __device__ constexpr uint32_t wl_entry(int j, uint32_t tier, int col) {
+  return (uint32_t)j | (tier << 8) | ((uint32_t)col << 16);
+}
 
 // Shared-memory layout after the W tier (byte offsets from the 1024-aligned base).
 struct SmemLayout {
-  int red, win, misc, h, a, total;
-  __host__ __device__ static SmemLayout make(int smem_w_bytes, int B, int r, int ra, bool recurrent) {
+  int red, win, misc, base, h, a, total;
+  __host__ __device__ static SmemLayout make(int smem_w_bytes, int B, int r, int ra, bool recurrent, int ng) {
     SmemLayout L;
     L.red = smem_w_bytes;                       // [kWarps][kMaxB] u64
     L.win = L.red + kWarps * kMaxB * 8;         // [kMaxB] int32
     L.misc = L.win + kMaxB * 4;                 // mbarrier u64, tmem addr u32, abort flag u32
-    L.h = L.misc + 16;                          // recurrent: [B][r] fp32
+    L.base = L.misc + 16;                       // [B][ng * 16] fp32: this step's base logits of the CTA's rows
+    L.h = L.base + B * ng * kGroupRows * 4;     // recurrent: [B][r] fp32
     L.a = L.h + (recurrent ? B * r * 4 : 0);    // recurrent: [ra][r] fp32
     L.total = L.a + (recurrent ? ra * r * 4 : 0);
     return L;
   }
 };
 
-// TMEM slot i of a CTA: lane quadrant i % 4, column block i / 4; the owning warp must sit on that
-// quadrant (warp % 4), which is how tcgen05.ld restricts lane access.
-__host__ __device__ inline int tmem_slot_warp(int i) { return (i & 3) + 4 * ((i >> 2) % (kWarps / 4)); }
-__host__ __device__ inline int tmem_slot_col(int i, int KB) { return (i >> 2) * 16 * KB; }
 
 // ------------------------------------------------------------------------------------------------
 // small device helpers
@@ -158,6 +164,18 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&a)[16]) {
                  "+r"(a[15])
                :
                : "memory");
+}
+
+// Waits for all of this thread's tcgen05.ld and ties every box's registers to the wait.
+template <int KB>
+__device__ __forceinline__ void tmem_wait_ld_boxes(uint32_t (&a)[KB][16]) {
+  tmem_wait_ld(a[0]);
+#pragma unroll
+  for (int bx = 1; bx < KB; ++bx)
+    asm volatile(""
+                 : "+r"(a[bx][0]), "+r"(a[bx][1]), "+r"(a[bx][2]), "+r"(a[bx][3]), "+r"(a[bx][4]), "+r"(a[bx][5]),
+                   "+r"(a[bx][6]), "+r"(a[bx][7]), "+r"(a[bx][8]), "+r"(a[bx][9]), "+r"(a[bx][10]), "+r"(a[bx][11]),
+                   "+r"(a[bx][12]), "+r"(a[bx][13]), "+r"(a[bx][14]), "+r"(a[bx][15]));
 }
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&a)[16]) {
@@ -221,6 +239,10 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t mbar, uint32_t parity
   }
 }
 
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) { return a > b ? a : b; }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -228,10 +250,11 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<const uint32_t*>(&p);
 }
 
-// Four mma ops of one 64-wide k box. a = [R0 | S0 | R1 | S1]: R rows g, S rows g+8, index 0/1 the two
+// Four mma ops of one 64-wide k box (see below). a = [R0 | S0 | R1 | S1]: R rows g, S rows g+8, index 0/1 the two
 // 16-byte chunks (2c, 2c+1) of the box. B fragments: 8 registers per box = 16 contiguous bf16 of the state.
+// The four ops of a box go to four independent accumulators so that they issue back to back.
 template <int KB, int NH>
-__device__ __forceinline__ void mma_box(float (&acc)[NH][4], const uint32_t (&a)[16],
+__device__ __forceinline__ void mma_box(float (&acc)[4][NH][4], const uint32_t (&a)[16],
                                         const uint32_t (&bf)[NH][KB][8], int bx) {
 #pragma unroll
   for (int rho = 0; rho < 2; ++rho) {
@@ -241,7 +264,7 @@ __device__ __forceinline__ void mma_box(float (&acc)[NH][4], const uint32_t (&a)
       const uint32_t a1 = a[8 * rho + 4 + 2 * h], a3 = a[8 * rho + 4 + 2 * h + 1];
 #pragma unroll
       for (int n = 0; n < NH; ++n)
-        mma_bf16_16816(acc[n], a0, a1, a2, a3, bf[n][bx][4 * rho + 2 * h], bf[n][bx][4 * rho + 2 * h + 1]);
+        mma_bf16_16816(acc[2 * rho + h][n], a0, a1, a2, a3, bf[n][bx][4 * rho + 2 * h], bf[n][bx][4 * rho + 2 * h + 1]);
     }
   }
 }
@@ -291,10 +314,35 @@ __device__ __forceinline__ void bfrag_from_bf16_row(uint32_t (&bf)[KB][8], const
   }
 }
 
+// Copies the base logits of step t for this CTA's rows into shared memory (coalesced; rows >= V read as
+// zero) using threads [first, first + count), and asks L2 for the rows of step t + 1.
+__device__ __forceinline__ void stage_base(const WalkArgs& P, float* s_base, int64_t row_base, int t, int first,
+                                           int count) {
+  const int rows = P.ng * kGroupRows;
+  const int i0 = (int)threadIdx.x - first;
+  if (i0 < 0 || i0 >= count || t >= P.gamma) return;
+  for (int i = i0; i < P.B * rows; i += count) {
+    const int n = i / rows, lr = i - n * rows;
+    const int64_t v = row_base + lr;
+    s_base[i] = (v < P.V) ? __ldg(P.base + ((int64_t)n * P.gamma + t) * P.V + v) : 0.f;
+  }
+  if (t + 1 < P.gamma) {
+    for (int i = i0 * 32; i < P.B * rows; i += count * 32) {
+      const int n = i / rows, lr = i - n * rows;
+      const int64_t v = row_base + lr;
+      if (v < P.V) prefetch_l2(P.base + ((int64_t)n * P.gamma + t + 1) * P.V + v);
+    }
+  }
+}
+
 // ------------------------------------------------------------------------------------------------
 // the kernel
 // ------------------------------------------------------------------------------------------------
-template <int KB, int NH>
+// KB: 64-wide boxes of the rank (r = 64 KB). NH: n8 halves of the batch (B <= 8 * NH). NB1: B == 1.
+// Warp roles: warps in rf_warp_mask keep one group in registers (plus shared-memory groups); the others
+// own the tensor-memory groups of their lane quadrant (plus shared-memory groups). The two roles run
+// separately compiled copies of the step loop so that neither pays for the other's registers.
+template <int KB, int NH, bool NB1>
 __global__ void __launch_bounds__(kThreads, 1)
     walk_kernel(const __grid_constant__ CUtensorMap tmapW, const __grid_constant__ WalkArgs P) {
   extern __shared__ uint8_t smem_raw[];
@@ -307,19 +355,24 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  const SmemLayout L = SmemLayout::make(P.smem_w_bytes, B, r, P.ra, recurrent);
+  const SmemLayout L = SmemLayout::make(P.smem_w_bytes, B, r, P.ra, recurrent, P.ng);
   uint8_t* sW = smem;
   unsigned long long* s_red = reinterpret_cast<unsigned long long*>(smem + L.red);
   int32_t* s_win = reinterpret_cast<int32_t*>(smem + L.win);
   unsigned long long* s_mbar = reinterpret_cast<unsigned long long*>(smem + L.misc);
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L.misc + 8);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L.misc + 12);
+  float* s_base = reinterpret_cast<float*>(smem + L.base);
   float* s_h = reinterpret_cast<float*>(smem + L.h);
   float* s_A = reinterpret_cast<float*>(smem + L.a);
 
   const uint32_t mbar = smem_u32(s_mbar);
   trace_stamp(P, 0);
   const int64_t row_base = (int64_t)cta * P.ng * kGroupRows;
+  const int rows_cta = P.ng * kGroupRows;
+  const int my_count = P.wl_count[warp];
+  const uint32_t my_entry = (lane < my_count) ? P.wl[warp][lane] : 0u;
+  const bool rf_warp = (P.rf_warp_mask >> warp) & 1u;
 
   // ---------------- set-up ----------------
   if (tid == 0) {
@@ -343,6 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tmem_fence_after();
   const uint32_t tmem_base = P.tmem_cols ? *s_tmem : 0u;
+  const uint32_t lane_quadrant = (uint32_t)(32 * (warp & 3)) << 16;
 
   // ---------------- entry: load the shard once (Fig. 4: the one-time shard load) ----------------
   if (tid == 0 && P.n_smem > 0) {
@@ -361,42 +415,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
+  stage_base(P, s_base, row_base, 0, 0, kThreads);
 
-  // tensor-memory groups of this warp: global -> registers -> tcgen05.st
-  const uint32_t lane_quadrant = (uint32_t)(32 * (warp & 3)) << 16;
-  for (int e = 0; e < P.wl_count[warp]; ++e) {
-    const int j = P.wl[warp][e];
-    if (j < P.n_smem || j >= P.n_smem + P.n_tmem) continue;
-    const int slot = j - P.n_smem;
-    const uint32_t taddr = tmem_base + lane_quadrant + (uint32_t)tmem_slot_col(slot, KB);
-    const int64_t v0 = row_base + (int64_t)kGroupRows * j + g;
+  // tensor-memory groups of this warp: global -> registers (all boxes of a group in flight) -> tcgen05.st
+  if (!rf_warp) {
+    for (int e = 0; e < my_count; ++e) {
+      const uint32_t ent = __shfl_sync(0xffffffffu, my_entry, e);
+      if (((ent >> 8) & 3u) != kTierTmem) continue;
+      const int j = (int)(ent & 0xFFu);
+      const uint32_t taddr = tmem_base + lane_quadrant + (ent >> 16);
+      const int64_t v0 = row_base + (int64_t)kGroupRows * j + g;
+      uint32_t a[KB][16];
 #pragma unroll
-    for (int bx = 0; bx < KB; ++bx) {
-      uint32_t a[16];
-      load_box_global(a, P.W, v0, V, r, bx, c);
-      tmem_st16(taddr + 16 * bx, a);
+      for (int bx = 0; bx < KB; ++bx) load_box_global(a[bx], P.W, v0, V, r, bx, c);
+#pragma unroll
+      for (int bx = 0; bx < KB; ++bx) tmem_st16(taddr + 16 * bx, a[bx]);
     }
   }
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-
-  // register-resident group (at most one per warp)
-  uint32_t rfA[(NH == 1) ? KB : 1][16];
-  int rf_group = -1;
-  if constexpr (NH == 1) {
-    for (int e = 0; e < P.wl_count[warp]; ++e) {
-      const int j = P.wl[warp][e];
-      if (j >= P.n_smem + P.n_tmem) rf_group = j;
-    }
-#pragma unroll
-    for (int bx = 0; bx < KB; ++bx) {
-      if (rf_group >= 0) {
-        load_box_global(rfA[bx], P.W, row_base + (int64_t)kGroupRows * rf_group + g, V, r, bx, c);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) rfA[bx][i] = 0u;
-      }
-    }
-  }
 
   // recurrent head: the initial state and this CTA's rows of A
   const int a_lo = cta * P.ra;
@@ -422,22 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   tmem_fence_after();
   trace_stamp(P, 1);
 
-  // ---------------- the walk ----------------
-  uint32_t bf[NH][KB][8];
-#pragma unroll
-  for (int h = 0; h < NH; ++h) {
-    const int n = 8 * h + g;
-    if (n < B) {
-      bfrag_from_f32<KB>(bf[h], recurrent ? (s_h + n * r) : (P.s0 + (int64_t)n * r), c);
-    } else {
-#pragma unroll
-      for (int bx = 0; bx < KB; ++bx)
-#pragma unroll
-        for (int i = 0; i < 8; ++i) bf[h][bx][i] = 0u;
-    }
-  }
-
-  const uint32_t sw_base = smem_u32(sW);
+  const uint8_t* sW_c = sW;
   const uint32_t box_stride = (uint32_t)(P.n_smem * kBoxBytes);
   const uint32_t off_rho0 = (uint32_t)(((2 * c) ^ g) << 4);
   const uint32_t off_rho1 = (uint32_t)(((2 * c + 1) ^ g) << 4);
@@ -445,206 +466,274 @@ __global__ void __launch_bounds__(kThreads, 1)
   const bool sampled = T > 0.0f;
   const bool want_f32 = (P.flags & kFlagLogitsF32) != 0u;
 
-  for (int t = 0; t < gamma; ++t) {
-    if (*s_abort) break;
-    const uint32_t tau = (uint32_t)(P.t0 + t);
-    trace_stamp(P, 2 + kTraceStampsPerStep * t);
-
-    // recurrent: this CTA's slice of A h_t, published with the step's arrival
-    if (recurrent && warp == 0) {
-      for (int p = 0; p < B * P.ra; ++p) {
-        const int n = p / P.ra, i = p % P.ra;
-        if (a_lo + i >= r) continue;
-        float s = 0.f;
-        for (int k = lane; k < r; k += 32) s = fmaf(s_A[i * r + k], s_h[n * r + k], s);
+  // ---------------- the walk ----------------
+  auto walk = [&](auto rf_tag) {
+    constexpr bool RFW = decltype(rf_tag)::value;
+    // register-resident group of this warp (RF warps only)
+    uint32_t rfA[RFW ? KB : 1][16];
+    if constexpr (RFW) {
+      int jr = -1;
+      for (int e = 0; e < my_count; ++e) {
+        const uint32_t ent = __shfl_sync(0xffffffffu, my_entry, e);
+        if (((ent >> 8) & 3u) == kTierRf) jr = (int)(ent & 0xFFu);
+      }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-        if (lane == 0) P.ah[((int64_t)(t & 1) * kMaxB + n) * r + a_lo + i] = s;
+      for (int bx = 0; bx < KB; ++bx) {
+        if (jr >= 0) {
+          load_box_global(rfA[bx], P.W, row_base + (int64_t)kGroupRows * jr + g, V, r, bx, c);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) rfA[bx][i] = 0u;
+        }
       }
     }
 
-    unsigned long long best[NH][2];
+    uint32_t bf[NH][KB][8];
 #pragma unroll
-    for (int h = 0; h < NH; ++h) best[h][0] = best[h][1] = 0ull;
-
-    for (int e = 0; e < P.wl_count[warp]; ++e) {
-      const int j = P.wl[warp][e];
-      const int64_t va = row_base + (int64_t)kGroupRows * j + g;
-
-      // base logits of this thread's rows and walks, loaded before the projection
-      float bv[NH][4];
-#pragma unroll
-      for (int h = 0; h < NH; ++h)
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int64_t v = va + ((q >> 1) << 3);
-          const int n = 8 * h + 2 * c + (q & 1);
-          bv[h][q] = (v < V && n < B) ? __ldg(P.base + ((int64_t)n * gamma + t) * V + v) : 0.f;
-        }
-
-      float acc[2][NH][4];
-#pragma unroll
-      for (int s = 0; s < 2; ++s)
-#pragma unroll
-        for (int h = 0; h < NH; ++h)
-#pragma unroll
-          for (int q = 0; q < 4; ++q) acc[s][h][q] = 0.f;
-
-      if (j < P.n_smem) {
-        const uint32_t row_addr = sw_base + (uint32_t)(kGroupRows * j + g) * 128u;
-#pragma unroll
-        for (int bx = 0; bx < KB; ++bx) {
-          uint32_t a[16];
-          const uint8_t* p = sW + (row_addr - sw_base) + bx * box_stride;
-          const uint4 r0 = *reinterpret_cast<const uint4*>(p + off_rho0);
-          const uint4 s0 = *reinterpret_cast<const uint4*>(p + 1024 + off_rho0);
-          const uint4 r1 = *reinterpret_cast<const uint4*>(p + off_rho1);
-          const uint4 s1 = *reinterpret_cast<const uint4*>(p + 1024 + off_rho1);
-          a[0] = r0.x; a[1] = r0.y; a[2] = r0.z; a[3] = r0.w;
-          a[4] = s0.x; a[5] = s0.y; a[6] = s0.z; a[7] = s0.w;
-          a[8] = r1.x; a[9] = r1.y; a[10] = r1.z; a[11] = r1.w;
-          a[12] = s1.x; a[13] = s1.y; a[14] = s1.z; a[15] = s1.w;
-          mma_box<KB, NH>(acc[bx & 1], a, bf, bx);
-        }
-      } else if (j < P.n_smem + P.n_tmem) {
-        const uint32_t taddr = tmem_base + lane_quadrant + (uint32_t)tmem_slot_col(j - P.n_smem, KB);
-#pragma unroll
-        for (int bx = 0; bx < KB; ++bx) {
-          uint32_t a[16];
-          tmem_ld16(a, taddr + 16 * bx);
-          tmem_wait_ld(a);
-          mma_box<KB, NH>(acc[bx & 1], a, bf, bx);
-        }
+    for (int h = 0; h < NH; ++h) {
+      const int n = 8 * h + g;
+      if (n < B) {
+        bfrag_from_f32<KB>(bf[h], recurrent ? (s_h + n * r) : (P.s0 + (int64_t)n * r), c);
       } else {
-        if constexpr (NH == 1) {
 #pragma unroll
-          for (int bx = 0; bx < KB; ++bx) mma_box<KB, NH>(acc[bx & 1], rfA[bx], bf, bx);
+        for (int bx = 0; bx < KB; ++bx)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) bf[h][bx][i] = 0u;
+      }
+    }
+
+    for (int t = 0; t < gamma; ++t) {
+      if (*s_abort) break;
+      const uint32_t tau = (uint32_t)(P.t0 + t);
+      trace_stamp(P, 2 + kTraceStampsPerStep * t);
+
+      // recurrent: this CTA's slice of A h_t, published with the step's arrival
+      if (recurrent && warp == 0) {
+        for (int p = 0; p < B * P.ra; ++p) {
+          const int n = p / P.ra, i = p % P.ra;
+          if (a_lo + i >= r) continue;
+          float s = 0.f;
+          for (int k = lane; k < r; k += 32) s = fmaf(s_A[i * r + k], s_h[n * r + k], s);
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+          if (lane == 0) P.ah[((int64_t)(t & 1) * kMaxB + n) * r + a_lo + i] = s;
         }
       }
 
-      // epilogue: z = p + base (fp32), optional emitted logit, selection key, running maximum
+      unsigned long long best[NH][2];
+#pragma unroll
+      for (int h = 0; h < NH; ++h) best[h][0] = best[h][1] = 0ull;
+
+      for (int e = 0; e < my_count; ++e) {
+        const uint32_t ent = __shfl_sync(0xffffffffu, my_entry, e);
+        const int j = (int)(ent & 0xFFu);
+        const uint32_t tier = (ent >> 8) & 3u;
+        const int64_t va = row_base + (int64_t)kGroupRows * j + g;
+
+        float acc[4][NH][4];
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+#pragma unroll
+          for (int h = 0; h < NH; ++h)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) acc[s][h][q] = 0.f;
+
+        if (tier == kTierSmem) {
+          const uint8_t* prow = sW_c + (uint32_t)(kGroupRows * j + g) * 128u;
+#pragma unroll
+          for (int bx = 0; bx < KB; ++bx) {
+            uint32_t a[16];
+            const uint8_t* p = prow + bx * box_stride;
+            const uint4 r0 = *reinterpret_cast<const uint4*>(p + off_rho0);
+            const uint4 s0 = *reinterpret_cast<const uint4*>(p + 1024 + off_rho0);
+            const uint4 r1 = *reinterpret_cast<const uint4*>(p + off_rho1);
+            const uint4 s1 = *reinterpret_cast<const uint4*>(p + 1024 + off_rho1);
+            a[0] = r0.x; a[1] = r0.y; a[2] = r0.z; a[3] = r0.w;
+            a[4] = s0.x; a[5] = s0.y; a[6] = s0.z; a[7] = s0.w;
+            a[8] = r1.x; a[9] = r1.y; a[10] = r1.z; a[11] = r1.w;
+            a[12] = s1.x; a[13] = s1.y; a[14] = s1.z; a[15] = s1.w;
+            mma_box<KB, NH>(acc, a, bf, bx);
+          }
+        } else if (tier == kTierTmem) {
+          if constexpr (!RFW) {
+            const uint32_t taddr = tmem_base + lane_quadrant + (ent >> 16);
+            // boxes read per wait: all of them for one batch half, two when both halves are live
+            constexpr int TB = (NH == 1 || KB < 4) ? KB : 2;
+#pragma unroll
+            for (int b0 = 0; b0 < KB; b0 += TB) {
+              uint32_t a[TB][16];
+#pragma unroll
+              for (int i = 0; i < TB; ++i) tmem_ld16(a[i], taddr + 16 * (b0 + i));
+              tmem_wait_ld_boxes<TB>(a);
+#pragma unroll
+              for (int i = 0; i < TB; ++i) mma_box<KB, NH>(acc, a[i], bf, b0 + i);
+            }
+          }
+        } else {
+          if constexpr (RFW) {
+#pragma unroll
+            for (int bx = 0; bx < KB; ++bx) mma_box<KB, NH>(acc, rfA[bx], bf, bx);
+          }
+        }
+
+        // epilogue: z = p + base (fp32), optional emitted logit, selection key, running maximum
+        if constexpr (NB1) {
+          if (c == 0) {
+#pragma unroll
+            for (int qq = 0; qq < 2; ++qq) {
+              const int64_t v = va + 8 * qq;
+              if (v < V) {
+                const int q = 2 * qq;
+                const float p = __fadd_rn(__fadd_rn(acc[0][0][q], acc[1][0][q]), __fadd_rn(acc[2][0][q], acc[3][0][q]));
+                const float z = __fadd_rn(p, s_base[kGroupRows * j + g + 8 * qq]);
+                const int64_t oi = (int64_t)t * V + v;
+                if (P.logits) {
+                  if (want_f32) reinterpret_cast<float*>(P.logits)[oi] = z;
+                  else reinterpret_cast<__nv_bfloat16*>(P.logits)[oi] = __float2bfloat16_rn(z);
+                }
+                float key = z;
+                if (sampled) key = __fadd_rn(__fdiv_rn(z, T), gumbel_noise(P.seed, 0u, tau, (uint32_t)v));
+                best[0][0] = umax64(best[0][0], pack_key(key, (uint32_t)v));
+              }
+            }
+          }
+        } else {
+#pragma unroll
+          for (int h = 0; h < NH; ++h)
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int64_t v = va + ((q >> 1) << 3);
+              const int n = 8 * h + 2 * c + (q & 1);
+              if (v < V && n < B) {
+                const float p =
+                    __fadd_rn(__fadd_rn(acc[0][h][q], acc[1][h][q]), __fadd_rn(acc[2][h][q], acc[3][h][q]));
+                const float z = __fadd_rn(p, s_base[n * rows_cta + kGroupRows * j + g + ((q >> 1) << 3)]);
+                const int64_t oi = ((int64_t)n * gamma + t) * V + v;
+                if (P.logits) {
+                  if (want_f32) reinterpret_cast<float*>(P.logits)[oi] = z;
+                  else reinterpret_cast<__nv_bfloat16*>(P.logits)[oi] = __float2bfloat16_rn(z);
+                }
+                float key = z;
+                if (sampled) key = __fadd_rn(__fdiv_rn(z, T), gumbel_noise(P.seed, (uint32_t)n, tau, (uint32_t)v));
+                best[h][q & 1] = umax64(best[h][q & 1], pack_key(key, (uint32_t)v));
+              }
+            }
+        }
+      }
+
+      // warp maximum over the 8 row positions g; lanes 0..3 then hold walks 8h + 2c and 8h + 2c + 1
 #pragma unroll
       for (int h = 0; h < NH; ++h)
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int64_t v = va + ((q >> 1) << 3);
-          const int n = 8 * h + 2 * c + (q & 1);
-          if (v < V && n < B) {
-            const float p = __fadd_rn(acc[0][h][q], acc[1][h][q]);
-            const float z = __fadd_rn(p, bv[h][q]);
-            const int64_t oi = ((int64_t)n * gamma + t) * V + v;
-            if (P.logits) {
-              if (want_f32) reinterpret_cast<float*>(P.logits)[oi] = z;
-              else reinterpret_cast<__nv_bfloat16*>(P.logits)[oi] = __float2bfloat16_rn(z);
-            }
-            float key = z;
-            if (sampled) key = __fadd_rn(__fdiv_rn(z, T), gumbel_noise(P.seed, (uint32_t)n, tau, (uint32_t)v));
-            best[h][q & 1] = umax64(best[h][q & 1], pack_key(key, (uint32_t)v));
-          }
+        for (int i = 0; i < 2; ++i) {
+          unsigned long long kk = best[h][i];
+          kk = umax64(kk, __shfl_xor_sync(0xffffffffu, kk, 4));
+          kk = umax64(kk, __shfl_xor_sync(0xffffffffu, kk, 8));
+          kk = umax64(kk, __shfl_xor_sync(0xffffffffu, kk, 16));
+          const int n = 8 * h + 2 * c + i;
+          if (g == 0 && n < B) s_red[warp * kMaxB + n] = kk;
         }
-    }
+      __syncthreads();
+      trace_stamp(P, 2 + kTraceStampsPerStep * t + 1);
 
-    // warp maximum over the 8 row positions g; lanes 0..3 then hold walks 8h + 2c and 8h + 2c + 1
-#pragma unroll
-    for (int h = 0; h < NH; ++h)
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        unsigned long long k = best[h][i];
-        k = umax64(k, __shfl_xor_sync(0xffffffffu, k, 4));
-        k = umax64(k, __shfl_xor_sync(0xffffffffu, k, 8));
-        k = umax64(k, __shfl_xor_sync(0xffffffffu, k, 16));
-        const int n = 8 * h + 2 * c + i;
-        if (g == 0 && n < B) s_red[warp * kMaxB + n] = k;
-      }
-    __syncthreads();
-    trace_stamp(P, 2 + kTraceStampsPerStep * t + 1);
+      // the other warps fetch the next step's base logits while warp 0 runs the exchange
+      stage_base(P, s_base, row_base, t + 1, 32, kThreads - 32);
 
-    // exchange (Fig. 8): CTA winner -> red.max into the step slot, release arrival, bounded acquire poll
-    if (warp == 0) {
-      unsigned long long k = 0ull;
-      if (lane < B)
-        for (int w = 0; w < kWarps; ++w) k = umax64(k, s_red[w * kMaxB + lane]);
-      unsigned long long* slot = P.slots + (int64_t)t * kMaxB;
-      for (int n = 0; n < B; ++n) {
-        const unsigned long long kn = __shfl_sync(0xffffffffu, k, n);
-        if (lane == 0 && kn != 0ull) asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(slot + n), "l"(kn) : "memory");
-      }
-      if (lane == 0) {
-        const bool skip = (P.flags & kFlagSkipArrival) && cta == 0 && t == 0;
-        if (!skip) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(P.cnt) : "memory");
-        const unsigned int target = (unsigned int)(t + 1) * (unsigned int)G;
-        const uint64_t t_start = globaltimer_ns();
-        uint32_t spins = 0;
-        while (true) {
-          unsigned int now;
-          asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(now) : "l"(P.cnt) : "memory");
-          if (now >= target) break;
-          if ((++spins & 31u) == 0u && globaltimer_ns() - t_start > P.timeout_ns) {
-            atomicCAS(P.status, 0, kStatusTimeout);
-            *s_abort = 1;
-            break;
-          }
+      // exchange (Fig. 8): CTA winner -> red.max into the step slot, release arrival, bounded acquire poll
+      if (warp == 0) {
+        unsigned long long kk = 0ull;
+        if (lane < B)
+          for (int w = 0; w < kWarps; ++w) kk = umax64(kk, s_red[w * kMaxB + lane]);
+        unsigned long long* slot = P.slots + (int64_t)t * kMaxB;
+        // the E row of this CTA's candidate goes to L2 now: if it wins, every CTA reads it right after the wait
+        if (lane < B && kk != 0ull && !(P.flags & kFlagFixedLatent)) {
+          const uint16_t* er = P.E + (int64_t)(0xFFFFFFFFu - (uint32_t)(kk & 0xFFFFFFFFull)) * r;
+          for (int off = 0; off < r * 2; off += 128) prefetch_l2(reinterpret_cast<const uint8_t*>(er) + off);
         }
-        trace_stamp(P, 2 + kTraceStampsPerStep * t + 2);
         for (int n = 0; n < B; ++n) {
-          unsigned long long kn;
-          asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(kn) : "l"(slot + n) : "memory");
-          const uint32_t x = 0xFFFFFFFFu - (uint32_t)(kn & 0xFFFFFFFFull);
-          s_win[n] = (int32_t)x;
-          if (cta == 0 && !*s_abort) P.tokens[(int64_t)n * gamma + t] = (int32_t)x;
+          const unsigned long long kn = __shfl_sync(0xffffffffu, kk, n);
+          if (lane == 0 && kn != 0ull)
+            asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(slot + n), "l"(kn) : "memory");
         }
-      }
-    }
-    __syncthreads();
-    if (*s_abort) break;
-
-    // winners must be rows of W (a failed exchange would show up here)
-    bool bad = false;
-    for (int n = 0; n < B; ++n) bad |= (s_win[n] < 0 || (int64_t)s_win[n] >= V);
-    if (bad) {
-      if (tid == 0) atomicCAS(P.status, 0, kStatusInternal);
-      break;
-    }
-
-    // ---------------- state advance ----------------
-    if (P.flags & kFlagFixedLatent) continue;
-    if (!recurrent) {
-#pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        const int n = 8 * h + g;
-        if (n < B) bfrag_from_bf16_row<KB>(bf[h], P.E + (int64_t)s_win[n] * r, c);
-      }
-      if (cta == 0 && P.state) {
-        for (int i = tid; i < B * r; i += kThreads) {
-          const int n = i / r, k = i % r;
-          const uint32_t bits = (uint32_t)P.E[(int64_t)s_win[n] * r + k] << 16;
-          P.state[((int64_t)n * gamma + t) * r + k] = __uint_as_float(bits);
+        if (lane == 0) {
+          const bool skip = (P.flags & kFlagSkipArrival) && cta == 0 && t == 0;
+          if (!skip) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(P.cnt) : "memory");
+          const unsigned int target = (unsigned int)(t + 1) * (unsigned int)G;
+          const uint64_t t_start = globaltimer_ns();
+          uint32_t spins = 0;
+          while (true) {
+            unsigned int now;
+            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(now) : "l"(P.cnt) : "memory");
+            if (now >= target) break;
+            if ((++spins & 31u) == 0u && globaltimer_ns() - t_start > P.timeout_ns) {
+              atomicCAS(P.status, 0, kStatusTimeout);
+              *s_abort = 1;
+              break;
+            }
+          }
+          trace_stamp(P, 2 + kTraceStampsPerStep * t + 2);
+          for (int n = 0; n < B; ++n) {
+            unsigned long long kn;
+            asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(kn) : "l"(slot + n) : "memory");
+            const uint32_t x = 0xFFFFFFFFu - (uint32_t)(kn & 0xFFFFFFFFull);
+            s_win[n] = (int32_t)x;
+            if (cta == 0 && !*s_abort) P.tokens[(int64_t)n * gamma + t] = (int32_t)x;
+          }
         }
-      }
-    } else {
-      const float* ah = P.ah + (int64_t)(t & 1) * kMaxB * r;
-      for (int i = tid; i < B * r; i += kThreads) {
-        const int n = i / r, k = i % r;
-        const float e = __uint_as_float((uint32_t)P.E[(int64_t)s_win[n] * r + k] << 16);
-        float pre = __fadd_rn(__ldcg(ah + n * r + k), e);
-        if (P.c) pre = __fadd_rn(pre, P.c[k]);
-        s_h[i] = tanhf(pre);
       }
       __syncthreads();
-#pragma unroll
-      for (int h = 0; h < NH; ++h) {
-        const int n = 8 * h + g;
-        if (n < B) bfrag_from_f32<KB>(bf[h], s_h + n * r, c);
+      if (*s_abort) break;
+
+      // winners must be rows of W (a failed exchange would show up here)
+      bool bad = false;
+      for (int n = 0; n < B; ++n) bad |= (s_win[n] < 0 || (int64_t)s_win[n] >= V);
+      if (bad) {
+        if (tid == 0) atomicCAS(P.status, 0, kStatusInternal);
+        break;
       }
-      if (cta == 0 && P.state) {
+
+      // ---------------- state advance ----------------
+      if (P.flags & kFlagFixedLatent) continue;
+      if (!recurrent) {
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          const int n = 8 * h + g;
+          if (n < B) bfrag_from_bf16_row<KB>(bf[h], P.E + (int64_t)s_win[n] * r, c);
+        }
+        if (cta == 0 && P.state) {
+          for (int i = tid; i < B * r; i += kThreads) {
+            const int n = i / r, k = i % r;
+            const uint32_t bits = (uint32_t)P.E[(int64_t)s_win[n] * r + k] << 16;
+            P.state[((int64_t)n * gamma + t) * r + k] = __uint_as_float(bits);
+          }
+        }
+      } else {
+        const float* ah = P.ah + (int64_t)(t & 1) * kMaxB * r;
         for (int i = tid; i < B * r; i += kThreads) {
           const int n = i / r, k = i % r;
-          P.state[((int64_t)n * gamma + t) * r + k] = s_h[i];
+          const float e = __uint_as_float((uint32_t)P.E[(int64_t)s_win[n] * r + k] << 16);
+          float pre = __fadd_rn(__ldcg(ah + n * r + k), e);
+          if (P.c) pre = __fadd_rn(pre, P.c[k]);
+          s_h[i] = tanhf(pre);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int h = 0; h < NH; ++h) {
+          const int n = 8 * h + g;
+          if (n < B) bfrag_from_f32<KB>(bf[h], s_h + n * r, c);
+        }
+        if (cta == 0 && P.state) {
+          for (int i = tid; i < B * r; i += kThreads) {
+            const int n = i / r, k = i % r;
+            P.state[((int64_t)n * gamma + t) * r + k] = s_h[i];
+          }
         }
       }
+      trace_stamp(P, 2 + kTraceStampsPerStep * t + 3);
     }
-    trace_stamp(P, 2 + kTraceStampsPerStep * t + 3);
-  }
+  };
+  if (rf_warp) walk(std::true_type{});
+  else walk(std::false_type{});
 
   // ---------------- exit ----------------
   // copies still in flight after a timed-out wait must land before the CTA's shared memory is released

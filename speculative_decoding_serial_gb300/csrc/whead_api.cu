@@ -22,8 +22,9 @@ struct Plan {
   int G = 0, ng = 0, n_smem = 0, n_tmem = 0, n_rf = 0, n_stream = 0;
   uint32_t tmem_cols = 0;
   int smem_bytes = 0, smem_w_bytes = 0, ra = 0, Bcap = 0;
+  uint32_t rf_warp_mask = 0;
   int32_t wl_count[kWarps] = {};
-  uint8_t wl[kWarps][kMaxWarpGroups] = {};
+  uint32_t wl[kWarps][kMaxWarpGroups] = {};
 };
 
 struct Scratch {
@@ -69,14 +70,14 @@ Plan make_plan(int64_t V, int r, int kind, int Bcap, int NH, int sm_count, int s
   const int64_t group_bytes = (int64_t)KB * kBoxBytes;
   const bool recurrent = kind == WHEAD_RECURRENT;
   const int tmem_max = 128 / KB;
-  const int rf_max = (NH == 1) ? kWarps : 0;
+  const int rf_max = (NH == 1) ? 8 : 0;  // at most two register warps per lane quadrant
 
   auto fits = [&](int G, Plan& out) -> bool {
     const int64_t ng64 = (ngt + G - 1) / G;
     if (ng64 > 255) return false;
     const int ng = (int)ng64;
     const int ra = recurrent ? (r + G - 1) / G : 0;
-    const SmemLayout L0 = SmemLayout::make(0, Bcap, r, ra, recurrent);
+    const SmemLayout L0 = SmemLayout::make(0, Bcap, r, ra, recurrent, ng);
     const int64_t fixed = 1024 + L0.total;
     const int64_t smem_groups_max = std::max<int64_t>(0, (smem_optin - fixed) / group_bytes);
     int n_smem = (int)std::min<int64_t>(ng, smem_groups_max);
@@ -95,34 +96,37 @@ Plan make_plan(int64_t V, int r, int kind, int Bcap, int NH, int sm_count, int s
     out.ra = ra;
     out.Bcap = Bcap;
     out.smem_w_bytes = (int)(n_smem * group_bytes);
-    out.smem_bytes = (int)(1024 + SmemLayout::make(out.smem_w_bytes, Bcap, r, ra, recurrent).total);
+    out.smem_bytes = (int)(1024 + SmemLayout::make(out.smem_w_bytes, Bcap, r, ra, recurrent, ng).total);
     if (n_tmem > 0) {
       const int cols = ((n_tmem - 1) / 4 + 1) * 16 * KB;
       uint32_t pw = 32;
       while ((int)pw < cols) pw <<= 1;
       out.tmem_cols = pw;
     }
-    // work lists
+    // work lists. Warp roles per lane quadrant q (warps q, q + 4, q + 8): the highest warps of a quadrant
+    // keep register-resident groups (one each), the rest own the quadrant's tensor-memory groups.
+    const int rf_per_q = (n_rf + 3) / 4;
+    const int tmem_warps_per_q = (kWarps / 4) - rf_per_q;
+    if (n_tmem > 0 && tmem_warps_per_q < 1) return false;
     int load[kWarps] = {};
     int sp_load[4] = {};
-    auto push = [&](int w, int j) -> bool {
+    auto push = [&](int w, uint32_t entry) -> bool {
       if (out.wl_count[w] >= kMaxWarpGroups) return false;
-      out.wl[w][out.wl_count[w]++] = (uint8_t)j;
+      out.wl[w][out.wl_count[w]++] = entry;
       load[w]++;
       sp_load[w & 3]++;
       return true;
     };
-    for (int i = 0; i < n_tmem; ++i)
-      if (!push(tmem_slot_warp(i), n_smem + i)) return false;
-    bool has_rf[kWarps] = {};
     for (int i = 0; i < n_rf; ++i) {
-      int best = -1;
-      for (int w = 0; w < kWarps; ++w)
-        if (!has_rf[w] && (best < 0 || sp_load[w & 3] < sp_load[best & 3] ||
-                           (sp_load[w & 3] == sp_load[best & 3] && load[w] < load[best])))
-          best = w;
-      has_rf[best] = true;
-      if (!push(best, n_smem + n_tmem + i)) return false;
+      const int q = i & 3, k = i >> 2;  // k-th register warp of quadrant q, counted from the top
+      const int w = q + 4 * ((kWarps / 4) - 1 - k);
+      out.rf_warp_mask |= 1u << w;
+      if (!push(w, wl_entry(n_smem + n_tmem + i, kTierRf, 0))) return false;
+    }
+    for (int i = 0; i < n_tmem; ++i) {
+      const int q = i & 3, idx = i >> 2;
+      const int w = q + 4 * (idx % tmem_warps_per_q);
+      if (!push(w, wl_entry(n_smem + i, kTierTmem, idx * 16 * KB))) return false;
     }
     for (int j = 0; j < n_smem; ++j) {
       int q = 0;
@@ -131,7 +135,7 @@ Plan make_plan(int64_t V, int r, int kind, int Bcap, int NH, int sm_count, int s
       int best = q;
       for (int w = q; w < kWarps; w += 4)
         if (load[w] < load[best]) best = w;
-      if (!push(best, j)) return false;
+      if (!push(best, wl_entry(j, kTierSmem, 0))) return false;
     }
     out.ok = true;
     return true;
@@ -164,9 +168,9 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-template <int KB, int NH>
+template <int KB, int NH, bool NB1>
 int launch_t(whead_t* h, const Plan& pl, const WalkArgs& a) {
-  auto fn = walk_kernel<KB, NH>;
+  auto fn = walk_kernel<KB, NH, NB1>;
   static int attr_bytes = 0;  // largest dynamic shared memory size granted so far (per instantiation)
   if (pl.smem_bytes > attr_bytes) {
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, h->smem_optin) != cudaSuccess)
@@ -187,17 +191,23 @@ int launch_t(whead_t* h, const Plan& pl, const WalkArgs& a) {
   return WHEAD_OK;
 }
 
+// Instantiation for (rank boxes, batch halves, single walk).
 int launch(whead_t* h, const Plan& pl, const WalkArgs& a, int NH) {
   const int KB = kb_of(h->p.r);
-  switch (KB * 2 + (NH - 1)) {
-    case 2: return launch_t<1, 1>(h, pl, a);
-    case 3: return launch_t<1, 2>(h, pl, a);
-    case 4: return launch_t<2, 1>(h, pl, a);
-    case 5: return launch_t<2, 2>(h, pl, a);
-    case 6: return launch_t<3, 1>(h, pl, a);
-    case 7: return launch_t<3, 2>(h, pl, a);
-    case 8: return launch_t<4, 1>(h, pl, a);
-    case 9: return launch_t<4, 2>(h, pl, a);
+  const bool one = a.B == 1;
+  switch (KB * 4 + (NH - 1) * 2 + (one ? 1 : 0)) {
+    case 4: return launch_t<1, 1, false>(h, pl, a);
+    case 5: return launch_t<1, 1, true>(h, pl, a);
+    case 6: return launch_t<1, 2, false>(h, pl, a);
+    case 8: return launch_t<2, 1, false>(h, pl, a);
+    case 9: return launch_t<2, 1, true>(h, pl, a);
+    case 10: return launch_t<2, 2, false>(h, pl, a);
+    case 12: return launch_t<3, 1, false>(h, pl, a);
+    case 13: return launch_t<3, 1, true>(h, pl, a);
+    case 14: return launch_t<3, 2, false>(h, pl, a);
+    case 16: return launch_t<4, 1, false>(h, pl, a);
+    case 17: return launch_t<4, 1, true>(h, pl, a);
+    case 18: return launch_t<4, 2, false>(h, pl, a);
     default: return WHEAD_ERR_UNSUPPORTED;
   }
 }
@@ -338,6 +348,7 @@ int whead_walk_ex(whead_t* h, const float* base, const float* s0, int32_t B, int
   a.tmem_cols = pl.tmem_cols;
   a.smem_w_bytes = pl.smem_w_bytes;
   a.ra = pl.ra;
+  a.rf_warp_mask = pl.rf_warp_mask;
   std::memcpy(a.wl_count, pl.wl_count, sizeof(a.wl_count));
   std::memcpy(a.wl, pl.wl, sizeof(a.wl));
   const int rc = launch(h, pl, a, NH);
@@ -479,9 +490,9 @@ int noalloc_setup(int dev, NaDevice** out) {
   return WHEAD_OK;
 }
 
-template <int KB, int NH>
+template <int KB, int NH, bool NB1>
 int noalloc_launch_t(const CUtensorMap& tmap, cudaStream_t stream, int smem_optin, const Plan& pl, const WalkArgs& a) {
-  auto fn = walk_kernel<KB, NH>;
+  auto fn = walk_kernel<KB, NH, NB1>;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin) != cudaSuccess)
     return WHEAD_ERR_CUDA;
   void* args[] = {(void*)&tmap, (void*)&a};
@@ -500,15 +511,19 @@ int noalloc_launch_t(const CUtensorMap& tmap, cudaStream_t stream, int smem_opti
 
 int noalloc_launch(int r, int NH, const CUtensorMap& tmap, cudaStream_t stream, int smem_optin, const Plan& pl,
                    const WalkArgs& a) {
-  switch (kb_of(r) * 2 + (NH - 1)) {
-    case 2: return noalloc_launch_t<1, 1>(tmap, stream, smem_optin, pl, a);
-    case 3: return noalloc_launch_t<1, 2>(tmap, stream, smem_optin, pl, a);
-    case 4: return noalloc_launch_t<2, 1>(tmap, stream, smem_optin, pl, a);
-    case 5: return noalloc_launch_t<2, 2>(tmap, stream, smem_optin, pl, a);
-    case 6: return noalloc_launch_t<3, 1>(tmap, stream, smem_optin, pl, a);
-    case 7: return noalloc_launch_t<3, 2>(tmap, stream, smem_optin, pl, a);
-    case 8: return noalloc_launch_t<4, 1>(tmap, stream, smem_optin, pl, a);
-    case 9: return noalloc_launch_t<4, 2>(tmap, stream, smem_optin, pl, a);
+  switch (kb_of(r) * 4 + (NH - 1) * 2 + (a.B == 1 ? 1 : 0)) {
+    case 4: return noalloc_launch_t<1, 1, false>(tmap, stream, smem_optin, pl, a);
+    case 5: return noalloc_launch_t<1, 1, true>(tmap, stream, smem_optin, pl, a);
+    case 6: return noalloc_launch_t<1, 2, false>(tmap, stream, smem_optin, pl, a);
+    case 8: return noalloc_launch_t<2, 1, false>(tmap, stream, smem_optin, pl, a);
+    case 9: return noalloc_launch_t<2, 1, true>(tmap, stream, smem_optin, pl, a);
+    case 10: return noalloc_launch_t<2, 2, false>(tmap, stream, smem_optin, pl, a);
+    case 12: return noalloc_launch_t<3, 1, false>(tmap, stream, smem_optin, pl, a);
+    case 13: return noalloc_launch_t<3, 1, true>(tmap, stream, smem_optin, pl, a);
+    case 14: return noalloc_launch_t<3, 2, false>(tmap, stream, smem_optin, pl, a);
+    case 16: return noalloc_launch_t<4, 1, false>(tmap, stream, smem_optin, pl, a);
+    case 17: return noalloc_launch_t<4, 1, true>(tmap, stream, smem_optin, pl, a);
+    case 18: return noalloc_launch_t<4, 2, false>(tmap, stream, smem_optin, pl, a);
     default: return WHEAD_ERR_UNSUPPORTED;
   }
 }
@@ -593,6 +608,7 @@ extern "C" int whead_walk_noalloc(const void* W, const void* E, const whead_para
   a.tmem_cols = pl.tmem_cols;
   a.smem_w_bytes = pl.smem_w_bytes;
   a.ra = pl.ra;
+  a.rf_warp_mask = pl.rf_warp_mask;
   std::memcpy(a.wl_count, pl.wl_count, sizeof(a.wl_count));
   std::memcpy(a.wl, pl.wl, sizeof(a.wl));
   return noalloc_launch(p.r, NH, tmap, stream, nd->smem_optin, pl, a);
