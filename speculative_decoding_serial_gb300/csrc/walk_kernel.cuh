@@ -148,12 +148,34 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// Same op with a zero accumulator input (starts a sum without zeroing registers first).
+__device__ __forceinline__ void mma_bf16_16816_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                                 uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
 __device__ __forceinline__ void tmem_ld16(uint32_t (&a)[16], uint32_t taddr) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
       : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3]), "=r"(a[4]), "=r"(a[5]), "=r"(a[6]), "=r"(a[7]),
         "=r"(a[8]), "=r"(a[9]), "=r"(a[10]), "=r"(a[11]), "=r"(a[12]), "=r"(a[13]), "=r"(a[14]), "=r"(a[15])
       : "r"(taddr));
+}
+
+// 64 columns of this warp's lane quadrant: the four boxes of one group in a single load.
+__device__ __forceinline__ void tmem_ld64(uint32_t (&a)[4][16], uint32_t taddr) {
+#define WH_R16(b) "=r"(a[b][0]), "=r"(a[b][1]), "=r"(a[b][2]), "=r"(a[b][3]), "=r"(a[b][4]), "=r"(a[b][5]), \
+    "=r"(a[b][6]), "=r"(a[b][7]), "=r"(a[b][8]), "=r"(a[b][9]), "=r"(a[b][10]), "=r"(a[b][11]), "=r"(a[b][12]), \
+    "=r"(a[b][13]), "=r"(a[b][14]), "=r"(a[b][15])
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+      : WH_R16(0), WH_R16(1), WH_R16(2), WH_R16(3)
+      : "r"(taddr));
+#undef WH_R16
 }
 
 // Waits for this thread's tcgen05.ld; the registers are tied to the wait so no use is scheduled before it.
@@ -263,8 +285,12 @@ __device__ __forceinline__ void mma_box(float (&acc)[4][NH][4], const uint32_t (
       const uint32_t a0 = a[8 * rho + 2 * h], a2 = a[8 * rho + 2 * h + 1];
       const uint32_t a1 = a[8 * rho + 4 + 2 * h], a3 = a[8 * rho + 4 + 2 * h + 1];
 #pragma unroll
-      for (int n = 0; n < NH; ++n)
-        mma_bf16_16816(acc[2 * rho + h][n], a0, a1, a2, a3, bf[n][bx][4 * rho + 2 * h], bf[n][bx][4 * rho + 2 * h + 1]);
+      for (int n = 0; n < NH; ++n) {
+        if (bx == 0)
+          mma_bf16_16816_z(acc[2 * rho + h][n], a0, a1, a2, a3, bf[n][bx][4 * rho + 2 * h], bf[n][bx][4 * rho + 2 * h + 1]);
+        else
+          mma_bf16_16816(acc[2 * rho + h][n], a0, a1, a2, a3, bf[n][bx][4 * rho + 2 * h], bf[n][bx][4 * rho + 2 * h + 1]);
+      }
     }
   }
 }
@@ -321,17 +347,13 @@ __device__ __forceinline__ void stage_base(const WalkArgs& P, float* s_base, int
   const int rows = P.ng * kGroupRows;
   const int i0 = (int)threadIdx.x - first;
   if (i0 < 0 || i0 >= count || t >= P.gamma) return;
-  for (int i = i0; i < P.B * rows; i += count) {
-    const int n = i / rows, lr = i - n * rows;
-    const int64_t v = row_base + lr;
-    s_base[i] = (v < P.V) ? __ldg(P.base + ((int64_t)n * P.gamma + t) * P.V + v) : 0.f;
-  }
-  if (t + 1 < P.gamma) {
-    for (int i = i0 * 32; i < P.B * rows; i += count * 32) {
-      const int n = i / rows, lr = i - n * rows;
-      const int64_t v = row_base + lr;
-      if (v < P.V) prefetch_l2(P.base + ((int64_t)n * P.gamma + t + 1) * P.V + v);
-    }
+  const int valid = (int)min((int64_t)rows, P.V - row_base);  // rows of this CTA below V (may be <= 0)
+  for (int n = 0; n < P.B; ++n) {
+    const float* src = P.base + ((int64_t)n * P.gamma + t) * P.V + row_base;
+    float* dst = s_base + n * rows;
+    for (int lr = i0; lr < rows; lr += count) dst[lr] = (lr < valid) ? __ldg(src + lr) : 0.f;
+    if (t + 1 < P.gamma)
+      for (int lr = 32 * i0; lr < valid; lr += 32 * count) prefetch_l2(src + P.V + lr);
   }
 }
 
@@ -405,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t dst0 = smem_u32(sW);
     for (int bx = 0; bx < KB; ++bx) {
       for (int j = 0; j < P.n_smem; ++j) {
-        const uint32_t dst = dst0 + (uint32_t)(bx * P.n_smem + j) * kBoxBytes;
+        const uint32_t dst = dst0 + (uint32_t)(j * KB + bx) * kBoxBytes;
         const int x = 64 * bx;
         const int y = (int)(row_base + (int64_t)kGroupRows * j);
         asm volatile(
@@ -459,7 +481,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   trace_stamp(P, 1);
 
   const uint8_t* sW_c = sW;
-  const uint32_t box_stride = (uint32_t)(P.n_smem * kBoxBytes);
   const uint32_t off_rho0 = (uint32_t)(((2 * c) ^ g) << 4);
   const uint32_t off_rho1 = (uint32_t)(((2 * c + 1) ^ g) << 4);
   const float T = P.T;
@@ -520,34 +541,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
 
-      unsigned long long best[NH][2];
-#pragma unroll
-      for (int h = 0; h < NH; ++h) best[h][0] = best[h][1] = 0ull;
-
       for (int e = 0; e < my_count; ++e) {
         const uint32_t ent = __shfl_sync(0xffffffffu, my_entry, e);
         const int j = (int)(ent & 0xFFu);
         const uint32_t tier = (ent >> 8) & 3u;
-        const int64_t va = row_base + (int64_t)kGroupRows * j + g;
 
         float acc[4][NH][4];
-#pragma unroll
-        for (int s = 0; s < 4; ++s)
-#pragma unroll
-          for (int h = 0; h < NH; ++h)
-#pragma unroll
-            for (int q = 0; q < 4; ++q) acc[s][h][q] = 0.f;
-
         if (tier == kTierSmem) {
-          const uint8_t* prow = sW_c + (uint32_t)(kGroupRows * j + g) * 128u;
+          // group-major boxes: box bx of group j at (j * KB + bx) * 2048; rows g and g + 8 of the group
+          const uint8_t* p = sW_c + (uint32_t)(j * KB) * kBoxBytes + (uint32_t)g * 128u;
 #pragma unroll
           for (int bx = 0; bx < KB; ++bx) {
             uint32_t a[16];
-            const uint8_t* p = prow + bx * box_stride;
-            const uint4 r0 = *reinterpret_cast<const uint4*>(p + off_rho0);
-            const uint4 s0 = *reinterpret_cast<const uint4*>(p + 1024 + off_rho0);
-            const uint4 r1 = *reinterpret_cast<const uint4*>(p + off_rho1);
-            const uint4 s1 = *reinterpret_cast<const uint4*>(p + 1024 + off_rho1);
+            const uint8_t* pb = p + bx * kBoxBytes;
+            const uint4 r0 = *reinterpret_cast<const uint4*>(pb + off_rho0);
+            const uint4 s0 = *reinterpret_cast<const uint4*>(pb + 1024 + off_rho0);
+            const uint4 r1 = *reinterpret_cast<const uint4*>(pb + off_rho1);
+            const uint4 s1 = *reinterpret_cast<const uint4*>(pb + 1024 + off_rho1);
             a[0] = r0.x; a[1] = r0.y; a[2] = r0.z; a[3] = r0.w;
             a[4] = s0.x; a[5] = s0.y; a[6] = s0.z; a[7] = s0.w;
             a[8] = r1.x; a[9] = r1.y; a[10] = r1.z; a[11] = r1.w;
@@ -557,82 +567,101 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (tier == kTierTmem) {
           if constexpr (!RFW) {
             const uint32_t taddr = tmem_base + lane_quadrant + (ent >> 16);
-            // boxes read per wait: all of them for one batch half, two when both halves are live
-            constexpr int TB = (NH == 1 || KB < 4) ? KB : 2;
+            if constexpr (KB == 4 && NH == 1) {
+              uint32_t a[4][16];
+              tmem_ld64(a, taddr);
+              tmem_wait_ld_boxes<4>(a);
 #pragma unroll
-            for (int b0 = 0; b0 < KB; b0 += TB) {
-              uint32_t a[TB][16];
+              for (int bx = 0; bx < 4; ++bx) mma_box<KB, NH>(acc, a[bx], bf, bx);
+            } else {
+              // boxes read per wait: all of them for one batch half, two when both halves are live
+              constexpr int TB = (NH == 1 || KB < 4) ? KB : 2;
 #pragma unroll
-              for (int i = 0; i < TB; ++i) tmem_ld16(a[i], taddr + 16 * (b0 + i));
-              tmem_wait_ld_boxes<TB>(a);
+              for (int b0 = 0; b0 < KB; b0 += TB) {
+                uint32_t a[TB][16];
 #pragma unroll
-              for (int i = 0; i < TB; ++i) mma_box<KB, NH>(acc, a[i], bf, b0 + i);
+                for (int i = 0; i < TB; ++i) tmem_ld16(a[i], taddr + 16 * (b0 + i));
+                tmem_wait_ld_boxes<TB>(a);
+#pragma unroll
+                for (int i = 0; i < TB; ++i) mma_box<KB, NH>(acc, a[i], bf, b0 + i);
+              }
             }
+          } else {
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+#pragma unroll
+              for (int h = 0; h < NH; ++h)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[s][h][q] = 0.f;
           }
         } else {
           if constexpr (RFW) {
 #pragma unroll
             for (int bx = 0; bx < KB; ++bx) mma_box<KB, NH>(acc, rfA[bx], bf, bx);
+          } else {
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+#pragma unroll
+              for (int h = 0; h < NH; ++h)
+#pragma unroll
+                for (int q = 0; q < 4; ++q) acc[s][h][q] = 0.f;
           }
         }
 
-        // epilogue: z = p + base (fp32), optional emitted logit, selection key, running maximum
+        // z = p + base: each (row, walk) of the group belongs to one lane, which adds its projection to
+        // the staged base logit in place (Fig. 7: projection summed, then added to the base logits)
+        const int lr0 = kGroupRows * j + g;
         if constexpr (NB1) {
           if (c == 0) {
-#pragma unroll
-            for (int qq = 0; qq < 2; ++qq) {
-              const int64_t v = va + 8 * qq;
-              if (v < V) {
-                const int q = 2 * qq;
-                const float p = __fadd_rn(__fadd_rn(acc[0][0][q], acc[1][0][q]), __fadd_rn(acc[2][0][q], acc[3][0][q]));
-                const float z = __fadd_rn(p, s_base[kGroupRows * j + g + 8 * qq]);
-                const int64_t oi = (int64_t)t * V + v;
-                if (P.logits) {
-                  if (want_f32) reinterpret_cast<float*>(P.logits)[oi] = z;
-                  else reinterpret_cast<__nv_bfloat16*>(P.logits)[oi] = __float2bfloat16_rn(z);
-                }
-                float key = z;
-                if (sampled) key = __fadd_rn(__fdiv_rn(z, T), gumbel_noise(P.seed, 0u, tau, (uint32_t)v));
-                best[0][0] = umax64(best[0][0], pack_key(key, (uint32_t)v));
-              }
-            }
+            s_base[lr0] = __fadd_rn(__fadd_rn(__fadd_rn(acc[0][0][0], acc[1][0][0]), __fadd_rn(acc[2][0][0], acc[3][0][0])),
+                                    s_base[lr0]);
+            s_base[lr0 + 8] =
+                __fadd_rn(__fadd_rn(__fadd_rn(acc[0][0][2], acc[1][0][2]), __fadd_rn(acc[2][0][2], acc[3][0][2])),
+                          s_base[lr0 + 8]);
           }
         } else {
 #pragma unroll
           for (int h = 0; h < NH; ++h)
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-              const int64_t v = va + ((q >> 1) << 3);
               const int n = 8 * h + 2 * c + (q & 1);
-              if (v < V && n < B) {
-                const float p =
-                    __fadd_rn(__fadd_rn(acc[0][h][q], acc[1][h][q]), __fadd_rn(acc[2][h][q], acc[3][h][q]));
-                const float z = __fadd_rn(p, s_base[n * rows_cta + kGroupRows * j + g + ((q >> 1) << 3)]);
-                const int64_t oi = ((int64_t)n * gamma + t) * V + v;
-                if (P.logits) {
-                  if (want_f32) reinterpret_cast<float*>(P.logits)[oi] = z;
-                  else reinterpret_cast<__nv_bfloat16*>(P.logits)[oi] = __float2bfloat16_rn(z);
-                }
-                float key = z;
-                if (sampled) key = __fadd_rn(__fdiv_rn(z, T), gumbel_noise(P.seed, (uint32_t)n, tau, (uint32_t)v));
-                best[h][q & 1] = umax64(best[h][q & 1], pack_key(key, (uint32_t)v));
+              if (n < B) {
+                const int idx = n * rows_cta + lr0 + ((q >> 1) << 3);
+                s_base[idx] = __fadd_rn(
+                    __fadd_rn(__fadd_rn(acc[0][h][q], acc[1][h][q]), __fadd_rn(acc[2][h][q], acc[3][h][q])), s_base[idx]);
               }
             }
         }
       }
+      __syncthreads();
 
-      // warp maximum over the 8 row positions g; lanes 0..3 then hold walks 8h + 2c and 8h + 2c + 1
-#pragma unroll
-      for (int h = 0; h < NH; ++h)
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          unsigned long long kk = best[h][i];
-          kk = umax64(kk, __shfl_xor_sync(0xffffffffu, kk, 4));
-          kk = umax64(kk, __shfl_xor_sync(0xffffffffu, kk, 8));
-          kk = umax64(kk, __shfl_xor_sync(0xffffffffu, kk, 16));
-          const int n = 8 * h + 2 * c + i;
-          if (g == 0 && n < B) s_red[warp * kMaxB + n] = kk;
+      // selection scan (Fig. 8, step 1): every thread scores rows of the CTA for one walk n = tid % Bp,
+      // emits the logits (coalesced) and keeps the largest packed key
+      {
+        const int Bp = B == 1 ? 1 : B == 2 ? 2 : B <= 4 ? 4 : B <= 8 ? 8 : 16;
+        const int n = tid & (Bp - 1);
+        const int stride = kThreads / Bp;
+        unsigned long long bestk = 0ull;
+        if (n < B) {
+          const float* zrow = s_base + n * rows_cta;
+          const int valid = (int)min((int64_t)rows_cta, V - row_base);
+          const int64_t obase = ((int64_t)n * gamma + t) * V + row_base;
+          for (int lr = tid / Bp; lr < valid; lr += stride) {
+            const float z = zrow[lr];
+            if (P.logits) {
+              if (want_f32) reinterpret_cast<float*>(P.logits)[obase + lr] = z;
+              else reinterpret_cast<__nv_bfloat16*>(P.logits)[obase + lr] = __float2bfloat16_rn(z);
+            }
+            const uint32_t v = (uint32_t)(row_base + lr);
+            float key = z;
+            if (sampled) key = __fadd_rn(__fdiv_rn(z, T), gumbel_noise(P.seed, (uint32_t)n, tau, v));
+            bestk = umax64(bestk, pack_key(key, v));
+          }
         }
+        for (int off = 16; off >= Bp; off >>= 1) bestk = umax64(bestk, __shfl_xor_sync(0xffffffffu, bestk, off));
+        if (lane < Bp && n < B) s_red[warp * kMaxB + n] = bestk;
+      }
+
       __syncthreads();
       trace_stamp(P, 2 + kTraceStampsPerStep * t + 1);
 
