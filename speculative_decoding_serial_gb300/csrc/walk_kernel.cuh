@@ -274,25 +274,39 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 
 // Four mma ops of one 64-wide k box (see below). a = [R0 | S0 | R1 | S1]: R rows g, S rows g+8, index 0/1 the two
 // 16-byte chunks (2c, 2c+1) of the box. B fragments: 8 registers per box = 16 contiguous bf16 of the state.
-// The four ops of a box go to four independent accumulators so that they issue back to back.
+// The four ops of a box go to four independent accumulators so that they issue back to back. The box's
+// A operands are stored in fragment order: a[4m .. 4m + 3] = {a0, a1, a2, a3} of op m (m = 2 rho + h), so
+// each op reads four consecutive registers as they were loaded.
 template <int KB, int NH>
 __device__ __forceinline__ void mma_box(float (&acc)[4][NH][4], const uint32_t (&a)[16],
                                         const uint32_t (&bf)[NH][KB][8], int bx) {
 #pragma unroll
-  for (int rho = 0; rho < 2; ++rho) {
+  for (int m = 0; m < 4; ++m) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const uint32_t a0 = a[8 * rho + 2 * h], a2 = a[8 * rho + 2 * h + 1];
-      const uint32_t a1 = a[8 * rho + 4 + 2 * h], a3 = a[8 * rho + 4 + 2 * h + 1];
-#pragma unroll
-      for (int n = 0; n < NH; ++n) {
-        if (bx == 0)
-          mma_bf16_16816_z(acc[2 * rho + h][n], a0, a1, a2, a3, bf[n][bx][4 * rho + 2 * h], bf[n][bx][4 * rho + 2 * h + 1]);
-        else
-          mma_bf16_16816(acc[2 * rho + h][n], a0, a1, a2, a3, bf[n][bx][4 * rho + 2 * h], bf[n][bx][4 * rho + 2 * h + 1]);
-      }
+    for (int n = 0; n < NH; ++n) {
+      if (bx == 0)
+        mma_bf16_16816_z(acc[m][n], a[4 * m], a[4 * m + 1], a[4 * m + 2], a[4 * m + 3], bf[n][bx][2 * m],
+                         bf[n][bx][2 * m + 1]);
+      else
+        mma_bf16_16816(acc[m][n], a[4 * m], a[4 * m + 1], a[4 * m + 2], a[4 * m + 3], bf[n][bx][2 * m],
+                       bf[n][bx][2 * m + 1]);
     }
   }
+}
+
+// Rows g / g + 8 of a box as loaded ([R0 | S0 | R1 | S1]: chunk 2c then 2c + 1 of each row) to fragment
+// order: op m = 2 rho + h takes {R_rho[2h], S_rho[2h], R_rho[2h + 1], S_rho[2h + 1]}.
+__device__ __forceinline__ void rows_to_fragments(uint32_t (&q)[16], const uint32_t (&a)[16]) {
+#pragma unroll
+  for (int rho = 0; rho < 2; ++rho)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int m = 2 * rho + h;
+      q[4 * m + 0] = a[8 * rho + 2 * h];
+      q[4 * m + 1] = a[8 * rho + 4 + 2 * h];
+      q[4 * m + 2] = a[8 * rho + 2 * h + 1];
+      q[4 * m + 3] = a[8 * rho + 4 + 2 * h + 1];
+    }
 }
 
 // A fragments of box bx of a group read straight from W in global memory (row-major, unswizzled):
@@ -451,7 +465,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int bx = 0; bx < KB; ++bx) load_box_global(a[bx], P.W, v0, V, r, bx, c);
 #pragma unroll
-      for (int bx = 0; bx < KB; ++bx) tmem_st16(taddr + 16 * bx, a[bx]);
+      for (int bx = 0; bx < KB; ++bx) {
+        uint32_t q[16];
+        rows_to_fragments(q, a[bx]);
+        tmem_st16(taddr + 16 * bx, q);
+      }
     }
   }
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
@@ -475,14 +493,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       *s_abort = 1;
     }
   }
+  // each warp turns whole boxes of the shared tier from the TMA layout (16 rows x 128 B, 128-byte swizzle:
+  // chunk ^ (row % 8)) into fragment order; a box is read completely into registers before it is rewritten
+  if (tma_done) {
+    const uint32_t off0 = (uint32_t)(((2 * c) ^ g) << 4), off1 = (uint32_t)(((2 * c + 1) ^ g) << 4);
+    for (int b = warp; b < P.n_smem * KB; b += kWarps) {
+      uint8_t* box = sW + (uint32_t)b * kBoxBytes;
+      const uint4 r0 = *reinterpret_cast<const uint4*>(box + g * 128 + off0);
+      const uint4 s0 = *reinterpret_cast<const uint4*>(box + (g + 8) * 128 + off0);
+      const uint4 r1 = *reinterpret_cast<const uint4*>(box + g * 128 + off1);
+      const uint4 s1 = *reinterpret_cast<const uint4*>(box + (g + 8) * 128 + off1);
+      __syncwarp();
+      uint4* out = reinterpret_cast<uint4*>(box) + lane;
+      out[0] = make_uint4(r0.x, s0.x, r0.y, s0.y);
+      out[32] = make_uint4(r0.z, s0.z, r0.w, s0.w);
+      out[64] = make_uint4(r1.x, s1.x, r1.y, s1.y);
+      out[96] = make_uint4(r1.z, s1.z, r1.w, s1.w);
+    }
+  }
   tmem_fence_before();
   __syncthreads();
   tmem_fence_after();
   trace_stamp(P, 1);
 
   const uint8_t* sW_c = sW;
-  const uint32_t off_rho0 = (uint32_t)(((2 * c) ^ g) << 4);
-  const uint32_t off_rho1 = (uint32_t)(((2 * c + 1) ^ g) << 4);
   const float T = P.T;
   const bool sampled = T > 0.0f;
   const bool want_f32 = (P.flags & kFlagLogitsF32) != 0u;
@@ -501,7 +535,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int bx = 0; bx < KB; ++bx) {
         if (jr >= 0) {
-          load_box_global(rfA[bx], P.W, row_base + (int64_t)kGroupRows * jr + g, V, r, bx, c);
+          uint32_t a[16];
+          load_box_global(a, P.W, row_base + (int64_t)kGroupRows * jr + g, V, r, bx, c);
+          rows_to_fragments(rfA[bx], a);
         } else {
 #pragma unroll
           for (int i = 0; i < 16; ++i) rfA[bx][i] = 0u;
@@ -548,20 +584,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         float acc[4][NH][4];
         if (tier == kTierSmem) {
-          // group-major boxes: box bx of group j at (j * KB + bx) * 2048; rows g and g + 8 of the group
-          const uint8_t* p = sW_c + (uint32_t)(j * KB) * kBoxBytes + (uint32_t)g * 128u;
+          // group-major boxes (box bx of group j at (j * KB + bx) * 2048), each stored as four lane-major
+          // 512-byte fragment blocks: one conflict-free 16-byte load per op
+          const uint8_t* p = sW_c + (uint32_t)(j * KB) * kBoxBytes + (uint32_t)lane * 16u;
 #pragma unroll
           for (int bx = 0; bx < KB; ++bx) {
             uint32_t a[16];
-            const uint8_t* pb = p + bx * kBoxBytes;
-            const uint4 r0 = *reinterpret_cast<const uint4*>(pb + off_rho0);
-            const uint4 s0 = *reinterpret_cast<const uint4*>(pb + 1024 + off_rho0);
-            const uint4 r1 = *reinterpret_cast<const uint4*>(pb + off_rho1);
-            const uint4 s1 = *reinterpret_cast<const uint4*>(pb + 1024 + off_rho1);
-            a[0] = r0.x; a[1] = r0.y; a[2] = r0.z; a[3] = r0.w;
-            a[4] = s0.x; a[5] = s0.y; a[6] = s0.z; a[7] = s0.w;
-            a[8] = r1.x; a[9] = r1.y; a[10] = r1.z; a[11] = r1.w;
-            a[12] = s1.x; a[13] = s1.y; a[14] = s1.z; a[15] = s1.w;
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+              const uint4 x = *reinterpret_cast<const uint4*>(p + bx * kBoxBytes + m * 512);
+              a[4 * m] = x.x; a[4 * m + 1] = x.y; a[4 * m + 2] = x.z; a[4 * m + 3] = x.w;
+            }
             mma_box<KB, NH>(acc, a, bf, bx);
           }
         } else if (tier == kTierTmem) {
