@@ -44,6 +44,7 @@ constexpr int kMaxGamma = 64;
 constexpr int kMaxWarpGroups = 32;
 constexpr int kGroupRows = 16;
 constexpr int kBoxBytes = kGroupRows * 128;  // one 16-row x 64-element bf16 box
+constexpr int kTmaChunkGroups = 8;           // groups per large TMA copy (128 rows x 64 elements)
 
 // device status codes (match the public WHEAD_ERR_* values)
 constexpr int kStatusTimeout = -4;
@@ -380,7 +381,8 @@ __device__ __forceinline__ void stage_base(const WalkArgs& P, float* s_base, int
 // separately compiled copies of the step loop so that neither pays for the other's registers.
 template <int KB, int NH, bool NB1>
 __global__ void __launch_bounds__(kThreads, 1)
-    walk_kernel(const __grid_constant__ CUtensorMap tmapW, const __grid_constant__ WalkArgs P) {
+    walk_kernel(const __grid_constant__ CUtensorMap tmapW, const __grid_constant__ CUtensorMap tmapW128,
+                const __grid_constant__ WalkArgs P) {
   extern __shared__ uint8_t smem_raw[];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = lane >> 2, c = lane & 3;
@@ -436,18 +438,30 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ---------------- entry: load the shard once (Fig. 4: the one-time shard load) ----------------
   if (tid == 0 && P.n_smem > 0) {
+    // box-major shared tier: box bx of local group j at (bx * n_smem + j) * 2048. Runs of 8 groups go in one
+    // 128-row copy, the remainder in 16-row copies.
     const uint32_t bytes = (uint32_t)(P.n_smem * KB * kBoxBytes);
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(bytes) : "memory");
     const uint32_t dst0 = smem_u32(sW);
+    const int full = P.n_smem / kTmaChunkGroups;
     for (int bx = 0; bx < KB; ++bx) {
-      for (int j = 0; j < P.n_smem; ++j) {
-        const uint32_t dst = dst0 + (uint32_t)(j * KB + bx) * kBoxBytes;
-        const int x = 64 * bx;
+      const int x = 64 * bx;
+      for (int j = 0; j < P.n_smem;) {
+        const uint32_t dst = dst0 + (uint32_t)(bx * P.n_smem + j) * kBoxBytes;
         const int y = (int)(row_base + (int64_t)kGroupRows * j);
-        asm volatile(
-            "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
-            "l"(reinterpret_cast<uint64_t>(&tmapW)), "r"(x), "r"(y), "r"(mbar)
-            : "memory");
+        if (j < full * kTmaChunkGroups) {
+          asm volatile(
+              "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+              "l"(reinterpret_cast<uint64_t>(&tmapW128)), "r"(x), "r"(y), "r"(mbar)
+              : "memory");
+          j += kTmaChunkGroups;
+        } else {
+          asm volatile(
+              "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+              "l"(reinterpret_cast<uint64_t>(&tmapW)), "r"(x), "r"(y), "r"(mbar)
+              : "memory");
+          j += 1;
+        }
       }
     }
   }
@@ -517,6 +531,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   trace_stamp(P, 1);
 
   const uint8_t* sW_c = sW;
+  const uint32_t box_stride = (uint32_t)(P.n_smem * kBoxBytes);
   const float T = P.T;
   const bool sampled = T > 0.0f;
   const bool want_f32 = (P.flags & kFlagLogitsF32) != 0u;
@@ -584,15 +599,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
         float acc[4][NH][4];
         if (tier == kTierSmem) {
-          // group-major boxes (box bx of group j at (j * KB + bx) * 2048), each stored as four lane-major
-          // 512-byte fragment blocks: one conflict-free 16-byte load per op
-          const uint8_t* p = sW_c + (uint32_t)(j * KB) * kBoxBytes + (uint32_t)lane * 16u;
+          // box-major shared tier (box bx of group j at (bx * n_smem + j) * 2048), each box stored as four
+          // lane-major 512-byte fragment blocks: one conflict-free 16-byte load per op
+          const uint8_t* p = sW_c + (uint32_t)j * kBoxBytes + (uint32_t)lane * 16u;
 #pragma unroll
           for (int bx = 0; bx < KB; ++bx) {
             uint32_t a[16];
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
-              const uint4 x = *reinterpret_cast<const uint4*>(p + bx * kBoxBytes + m * 512);
+              const uint4 x = *reinterpret_cast<const uint4*>(p + bx * box_stride + m * 512);
               a[4 * m] = x.x; a[4 * m + 1] = x.y; a[4 * m + 2] = x.z; a[4 * m + 3] = x.w;
             }
             mma_box<KB, NH>(acc, a, bf, bx);

@@ -42,7 +42,8 @@ struct whead_s {
   whead_params p{};
   const uint16_t* W = nullptr;
   const uint16_t* E = nullptr;
-  CUtensorMap tmap{};
+  CUtensorMap tmap{};     // W: 64 x 16 boxes
+  CUtensorMap tmap128{};  // W: 64 x 128 boxes
   int sm_count = 0, smem_optin = 0;
   Plan plan[2];  // walks <= 8, walks <= 16
   void* scratch_block = nullptr;
@@ -177,7 +178,7 @@ int launch_t(whead_t* h, const Plan& pl, const WalkArgs& a) {
       return WHEAD_ERR_CUDA;
     attr_bytes = h->smem_optin;
   }
-  void* args[] = {(void*)&h->tmap, (void*)&a};
+  void* args[] = {(void*)&h->tmap, (void*)&h->tmap128, (void*)&a};
   cudaError_t e = cudaLaunchCooperativeKernel((const void*)fn, dim3(pl.G), dim3(kThreads), args, (size_t)pl.smem_bytes,
                                               h->stream);
   if (e == cudaErrorCooperativeLaunchTooLarge) {
@@ -213,6 +214,21 @@ int launch(whead_t* h, const Plan& pl, const WalkArgs& a, int NH) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// TMA descriptor of W (2-D: r elements inner, V rows) with 64-element x `rows` boxes, 128-byte swizzle and
+// zero fill outside the tensor.
+int encode_w(CUtensorMap* m, const void* W, int64_t V, int r, int rows) {
+  auto encode = get_encode();
+  if (!encode) return WHEAD_ERR_CUDA;
+  cuuint64_t gdim[2] = {(cuuint64_t)r, (cuuint64_t)V};
+  cuuint64_t gstride[1] = {(cuuint64_t)r * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)rows};
+  cuuint32_t estride[2] = {1, 1};
+  CUresult cr = encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W), gdim, gstride, box, estride,
+                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return cr == CUDA_SUCCESS ? WHEAD_OK : WHEAD_ERR_CUDA;
+}
 
 }  // namespace
 
@@ -271,17 +287,9 @@ int whead_create(const void* W, const void* E, const whead_params* params, whead
     if (!h->plan[1].ok) return fail(WHEAD_ERR_UNSUPPORTED);
   }
 
-  // TMA descriptor of W: 2-D (r elements inner, V rows), 64 x 16 boxes, 128-byte swizzle, zero fill
-  auto encode = get_encode();
-  if (!encode) return fail(WHEAD_ERR_CUDA);
-  cuuint64_t gdim[2] = {(cuuint64_t)p.r, (cuuint64_t)p.V};
-  cuuint64_t gstride[1] = {(cuuint64_t)p.r * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)kGroupRows};
-  cuuint32_t estride[2] = {1, 1};
-  CUresult cr = encode(&h->tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W), gdim, gstride, box, estride,
-                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (cr != CUDA_SUCCESS) return fail(WHEAD_ERR_CUDA);
+  // TMA descriptors of W: 64 x 16 and 64 x 128 boxes
+  if (encode_w(&h->tmap, W, p.V, p.r, kGroupRows) != WHEAD_OK) return fail(WHEAD_ERR_CUDA);
+  if (encode_w(&h->tmap128, W, p.V, p.r, kGroupRows * kTmaChunkGroups) != WHEAD_OK) return fail(WHEAD_ERR_CUDA);
 
   // scratch: exchange slots (two parities), two counters on their own lines, A h slices, status word
   const size_t slots_bytes = 2 * (size_t)kMaxGamma * kMaxB * 8;
@@ -491,11 +499,12 @@ int noalloc_setup(int dev, NaDevice** out) {
 }
 
 template <int KB, int NH, bool NB1>
-int noalloc_launch_t(const CUtensorMap& tmap, cudaStream_t stream, int smem_optin, const Plan& pl, const WalkArgs& a) {
+int noalloc_launch_t(const CUtensorMap& tmap, const CUtensorMap& tmap128, cudaStream_t stream, int smem_optin,
+                     const Plan& pl, const WalkArgs& a) {
   auto fn = walk_kernel<KB, NH, NB1>;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin) != cudaSuccess)
     return WHEAD_ERR_CUDA;
-  void* args[] = {(void*)&tmap, (void*)&a};
+  void* args[] = {(void*)&tmap, (void*)&tmap128, (void*)&a};
   cudaError_t e = cudaLaunchCooperativeKernel((const void*)fn, dim3(pl.G), dim3(kThreads), args, (size_t)pl.smem_bytes,
                                               stream);
   if (e == cudaErrorCooperativeLaunchTooLarge) {
@@ -509,21 +518,21 @@ int noalloc_launch_t(const CUtensorMap& tmap, cudaStream_t stream, int smem_opti
   return WHEAD_OK;
 }
 
-int noalloc_launch(int r, int NH, const CUtensorMap& tmap, cudaStream_t stream, int smem_optin, const Plan& pl,
-                   const WalkArgs& a) {
+int noalloc_launch(int r, int NH, const CUtensorMap& tmap, const CUtensorMap& tmap128, cudaStream_t stream,
+                   int smem_optin, const Plan& pl, const WalkArgs& a) {
   switch (kb_of(r) * 4 + (NH - 1) * 2 + (a.B == 1 ? 1 : 0)) {
-    case 4: return noalloc_launch_t<1, 1, false>(tmap, stream, smem_optin, pl, a);
-    case 5: return noalloc_launch_t<1, 1, true>(tmap, stream, smem_optin, pl, a);
-    case 6: return noalloc_launch_t<1, 2, false>(tmap, stream, smem_optin, pl, a);
-    case 8: return noalloc_launch_t<2, 1, false>(tmap, stream, smem_optin, pl, a);
-    case 9: return noalloc_launch_t<2, 1, true>(tmap, stream, smem_optin, pl, a);
-    case 10: return noalloc_launch_t<2, 2, false>(tmap, stream, smem_optin, pl, a);
-    case 12: return noalloc_launch_t<3, 1, false>(tmap, stream, smem_optin, pl, a);
-    case 13: return noalloc_launch_t<3, 1, true>(tmap, stream, smem_optin, pl, a);
-    case 14: return noalloc_launch_t<3, 2, false>(tmap, stream, smem_optin, pl, a);
-    case 16: return noalloc_launch_t<4, 1, false>(tmap, stream, smem_optin, pl, a);
-    case 17: return noalloc_launch_t<4, 1, true>(tmap, stream, smem_optin, pl, a);
-    case 18: return noalloc_launch_t<4, 2, false>(tmap, stream, smem_optin, pl, a);
+    case 4: return noalloc_launch_t<1, 1, false>(tmap, tmap128, stream, smem_optin, pl, a);
+    case 5: return noalloc_launch_t<1, 1, true>(tmap, tmap128, stream, smem_optin, pl, a);
+    case 6: return noalloc_launch_t<1, 2, false>(tmap, tmap128, stream, smem_optin, pl, a);
+    case 8: return noalloc_launch_t<2, 1, false>(tmap, tmap128, stream, smem_optin, pl, a);
+    case 9: return noalloc_launch_t<2, 1, true>(tmap, tmap128, stream, smem_optin, pl, a);
+    case 10: return noalloc_launch_t<2, 2, false>(tmap, tmap128, stream, smem_optin, pl, a);
+    case 12: return noalloc_launch_t<3, 1, false>(tmap, tmap128, stream, smem_optin, pl, a);
+    case 13: return noalloc_launch_t<3, 1, true>(tmap, tmap128, stream, smem_optin, pl, a);
+    case 14: return noalloc_launch_t<3, 2, false>(tmap, tmap128, stream, smem_optin, pl, a);
+    case 16: return noalloc_launch_t<4, 1, false>(tmap, tmap128, stream, smem_optin, pl, a);
+    case 17: return noalloc_launch_t<4, 1, true>(tmap, tmap128, stream, smem_optin, pl, a);
+    case 18: return noalloc_launch_t<4, 2, false>(tmap, tmap128, stream, smem_optin, pl, a);
     default: return WHEAD_ERR_UNSUPPORTED;
   }
 }
@@ -557,17 +566,9 @@ extern "C" int whead_walk_noalloc(const void* W, const void* E, const whead_para
   const Plan pl = make_plan(p.V, p.r, p.kind, B, NH, nd->sm_count, nd->smem_optin, 0);
   if (!pl.ok) return WHEAD_ERR_UNSUPPORTED;
 
-  auto encode = get_encode();
-  if (!encode) return WHEAD_ERR_CUDA;
-  CUtensorMap tmap;
-  cuuint64_t gdim[2] = {(cuuint64_t)p.r, (cuuint64_t)p.V};
-  cuuint64_t gstride[1] = {(cuuint64_t)p.r * 2};
-  cuuint32_t box[2] = {64, (cuuint32_t)kGroupRows};
-  cuuint32_t estride[2] = {1, 1};
-  if (encode(&tmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(W), gdim, gstride, box, estride,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-    return WHEAD_ERR_CUDA;
+  CUtensorMap tmap, tmap128;
+  if (encode_w(&tmap, W, p.V, p.r, kGroupRows) != WHEAD_OK) return WHEAD_ERR_CUDA;
+  if (encode_w(&tmap128, W, p.V, p.r, kGroupRows * kTmaChunkGroups) != WHEAD_OK) return WHEAD_ERR_CUDA;
 
   cudaStream_t stream = static_cast<cudaStream_t>(p.stream);
   uint8_t* sc = static_cast<uint8_t*>(nd->scratch);
@@ -611,5 +612,5 @@ extern "C" int whead_walk_noalloc(const void* W, const void* E, const whead_para
   a.rf_warp_mask = pl.rf_warp_mask;
   std::memcpy(a.wl_count, pl.wl_count, sizeof(a.wl_count));
   std::memcpy(a.wl, pl.wl, sizeof(a.wl));
-  return noalloc_launch(p.r, NH, tmap, stream, nd->smem_optin, pl, a);
+  return noalloc_launch(p.r, NH, tmap, tmap128, stream, nd->smem_optin, pl, a);
 }
