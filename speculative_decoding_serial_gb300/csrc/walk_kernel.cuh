@@ -165,6 +165,19 @@ __device__ __forceinline__ void tmem_ld16(uint32_t (&a)[16], uint32_t taddr) {
       : "r"(taddr));
 }
 
+// 32 columns of this warp's lane quadrant: two boxes of one group.
+__device__ __forceinline__ void tmem_ld32(uint32_t (&a)[2][16], uint32_t taddr) {
+#define WH_R16(b) "=r"(a[b][0]), "=r"(a[b][1]), "=r"(a[b][2]), "=r"(a[b][3]), "=r"(a[b][4]), "=r"(a[b][5]), \
+    "=r"(a[b][6]), "=r"(a[b][7]), "=r"(a[b][8]), "=r"(a[b][9]), "=r"(a[b][10]), "=r"(a[b][11]), "=r"(a[b][12]), \
+    "=r"(a[b][13]), "=r"(a[b][14]), "=r"(a[b][15])
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : WH_R16(0), WH_R16(1)
+      : "r"(taddr));
+#undef WH_R16
+}
+
 // 64 columns of this warp's lane quadrant: the four boxes of one group in a single load.
 __device__ __forceinline__ void tmem_ld64(uint32_t (&a)[4][16], uint32_t taddr) {
 #define WH_R16(b) "=r"(a[b][0]), "=r"(a[b][1]), "=r"(a[b][2]), "=r"(a[b][3]), "=r"(a[b][4]), "=r"(a[b][5]), \
@@ -260,6 +273,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t mbar, uint32_t parity
     if (done) return true;
     if (globaltimer_ns() - t_start > timeout_ns) return false;
   }
+}
+
+// s[i] += x as a shared-memory reduction (no result returned, so the issuing warp does not wait for it).
+__device__ __forceinline__ void red_add_shared(float* s, float x) {
+  asm volatile("red.shared.add.f32 [%0], %1;" ::"r"(smem_u32(s)), "f"(x) : "memory");
 }
 
 __device__ __forceinline__ void prefetch_l2(const void* p) {
@@ -616,11 +634,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           if constexpr (!RFW) {
             const uint32_t taddr = tmem_base + lane_quadrant + (ent >> 16);
             if constexpr (KB == 4 && NH == 1) {
-              uint32_t a[4][16];
-              tmem_ld64(a, taddr);
-              tmem_wait_ld_boxes<4>(a);
-#pragma unroll
-              for (int bx = 0; bx < 4; ++bx) mma_box<KB, NH>(acc, a[bx], bf, bx);
+              uint32_t a0[2][16], a1[2][16];
+              tmem_ld32(a0, taddr);
+              tmem_wait_ld_boxes<2>(a0);
+              tmem_ld32(a1, taddr + 32);
+              mma_box<KB, NH>(acc, a0[0], bf, 0);
+              mma_box<KB, NH>(acc, a0[1], bf, 1);
+              tmem_wait_ld_boxes<2>(a1);
+              mma_box<KB, NH>(acc, a1[0], bf, 2);
+              mma_box<KB, NH>(acc, a1[1], bf, 3);
             } else {
               // boxes read per wait: all of them for one batch half, two when both halves are live
               constexpr int TB = (NH == 1 || KB < 4) ? KB : 2;
@@ -685,7 +707,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // selection scan (Fig. 8, step 1): every thread scores rows of the CTA for one walk n = tid % Bp,
       // emits the logits (coalesced) and keeps the largest packed key
-      {
+      if constexpr (NB1) {
+        const int valid = (int)min((int64_t)rows_cta, V - row_base);
+        const int64_t obase = (int64_t)t * V + row_base;
+        unsigned long long bestk = 0ull;
+        for (int lr = tid; lr < valid; lr += kThreads) {
+          const float z = s_base[lr];
+          if (P.logits) {
+            if (want_f32) reinterpret_cast<float*>(P.logits)[obase + lr] = z;
+            else reinterpret_cast<__nv_bfloat16*>(P.logits)[obase + lr] = __float2bfloat16_rn(z);
+          }
+          const uint32_t v = (uint32_t)(row_base + lr);
+          float key = z;
+          if (sampled) key = __fadd_rn(__fdiv_rn(z, T), gumbel_noise(P.seed, 0u, tau, v));
+          bestk = umax64(bestk, pack_key(key, v));
+        }
+        uint32_t hi = (uint32_t)(bestk >> 32), lo = (uint32_t)bestk;
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+          const uint32_t ohi = __shfl_xor_sync(0xffffffffu, hi, off), olo = __shfl_xor_sync(0xffffffffu, lo, off);
+          const bool take = (ohi > hi) || (ohi == hi && olo > lo);
+          hi = take ? ohi : hi;
+          lo = take ? olo : lo;
+        }
+        if (lane == 0) s_red[warp * kMaxB] = ((unsigned long long)hi << 32) | lo;
+      } else {
         const int Bp = B == 1 ? 1 : B == 2 ? 2 : B <= 4 ? 4 : B <= 8 ? 8 : 16;
         const int n = tid & (Bp - 1);
         const int stride = kThreads / Bp;
