@@ -42,6 +42,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kMaxB = 16;
 constexpr int kMaxGamma = 64;
 constexpr int kMaxWarpGroups = 32;
+constexpr int kMaxGrid = 256;  // CTAs per walk: the exchange reads up to 8 slots per lane of one warp
 constexpr int kGroupRows = 16;
 constexpr int kBoxBytes = kGroupRows * 128;  // one 16-row x 64-element bf16 box
 constexpr int kTmaChunkGroups = 8;           // groups per large TMA copy (128 rows x 64 elements)
@@ -64,10 +65,11 @@ struct WalkArgs {
   int32_t* tokens;
   void* logits;
   float* state;
-  unsigned long long* slots;        // [kMaxGamma][kMaxB] for this call
+  unsigned long long* slots;        // [2 step parities][grid][B] tagged keys for this call
   unsigned int* cnt;                // arrival counter for this call
-  unsigned long long* slots_reset;  // the other call parity: cleared during this call
+  unsigned long long* slots_reset;  // the other call parity (or null): cleared during this call
   unsigned int* cnt_reset;
+  int32_t slots_reset_count;        // words to clear at slots_reset
   float* ah;                        // [2][kMaxB][r]: slices of A h exchanged between CTAs
   int* status;
   unsigned long long* trace;  // optional phase stamps: [grid][trace_stride] (clock64 half, globaltimer half)
@@ -444,8 +446,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   // clear the exchange words of the other call parity (the previous call on this stream has finished)
-  if (cta == G - 1) {
-    for (int i = tid; i < kMaxGamma * kMaxB; i += kThreads) P.slots_reset[i] = 0ull;
+  if (cta == G - 1 && P.slots_reset != nullptr) {
+    for (int i = tid; i < P.slots_reset_count; i += kThreads) P.slots_reset[i] = 0ull;
     if (tid == 0) *P.cnt_reset = 0u;
   }
   tmem_fence_before();
@@ -762,47 +764,95 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the other warps fetch the next step's base logits while warp 0 runs the exchange
       stage_base(P, s_base, row_base, t + 1, 32, kThreads - 32);
 
-      // exchange (Fig. 8): CTA winner -> red.max into the step slot, release arrival, bounded acquire poll
+      // exchange (Fig. 8). Each CTA publishes its winner for walk n as one 64-bit word in its own slot,
+      // tag (step + 1) << 56 | ord(key) << 24 | (2^24 - 1 - row), with a relaxed store: an aligned 64-bit store
+      // is single-copy atomic, so a reader sees the old word or the new one and the tag says which. A relaxed
+      // arrival count tells the readers when to look; a reader re-reads any slot whose tag is not yet this
+      // step's. No fence is needed because the answer is taken only from words that carry this step's tag.
+      // Slots alternate between two step buffers: a CTA can reach step t + 2 only after every CTA has
+      // arrived at step t + 1, that is, after every CTA has finished reading step t's buffer.
       if (warp == 0) {
         unsigned long long kk = 0ull;
         if (lane < B)
           for (int w = 0; w < kWarps; ++w) kk = umax64(kk, s_red[w * kMaxB + lane]);
-        unsigned long long* slot = P.slots + (int64_t)t * kMaxB;
         // the E row of this CTA's candidate goes to L2 now: if it wins, every CTA reads it right after the wait
         if (lane < B && kk != 0ull && !(P.flags & kFlagFixedLatent)) {
           const uint16_t* er = P.E + (int64_t)(0xFFFFFFFFu - (uint32_t)(kk & 0xFFFFFFFFull)) * r;
           for (int off = 0; off < r * 2; off += 128) prefetch_l2(reinterpret_cast<const uint8_t*>(er) + off);
         }
-        for (int n = 0; n < B; ++n) {
-          const unsigned long long kn = __shfl_sync(0xffffffffu, kk, n);
-          if (lane == 0 && kn != 0ull)
-            asm volatile("red.relaxed.gpu.global.max.u64 [%0], %1;" ::"l"(slot + n), "l"(kn) : "memory");
+        unsigned long long* sl = P.slots + (int64_t)(t & 1) * G * B;
+        const unsigned long long tag = (unsigned long long)(t + 1) << 56;
+        const bool skip = (P.flags & kFlagSkipArrival) && cta == 0 && t == 0;
+        if (lane < B && !skip) {
+          unsigned long long k56 = 0ull;
+          if (kk != 0ull) {
+            const uint32_t v = 0xFFFFFFFFu - (uint32_t)(kk & 0xFFFFFFFFull);
+            k56 = ((kk >> 32) << 24) | (unsigned long long)(0xFFFFFFu - v);
+          }
+          asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(sl + (int64_t)cta * B + lane), "l"(tag | k56) : "memory");
         }
+        __syncwarp();
+        const uint64_t t_start = globaltimer_ns();
         if (lane == 0) {
-          const bool skip = (P.flags & kFlagSkipArrival) && cta == 0 && t == 0;
-          if (!skip) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(P.cnt) : "memory");
+          if (!skip) asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(P.cnt) : "memory");
           const unsigned int target = (unsigned int)(t + 1) * (unsigned int)G;
-          const uint64_t t_start = globaltimer_ns();
           uint32_t spins = 0;
           while (true) {
             unsigned int now;
-            asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(now) : "l"(P.cnt) : "memory");
+            asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(now) : "l"(P.cnt) : "memory");
             if (now >= target) break;
             if ((++spins & 31u) == 0u && globaltimer_ns() - t_start > P.timeout_ns) {
-              atomicCAS(P.status, 0, kStatusTimeout);
               *s_abort = 1;
               break;
             }
           }
-          trace_stamp(P, 2 + kTraceStampsPerStep * t + 2);
-          for (int n = 0; n < B; ++n) {
-            unsigned long long kn;
-            asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(kn) : "l"(slot + n) : "memory");
-            const uint32_t x = 0xFFFFFFFFu - (uint32_t)(kn & 0xFFFFFFFFull);
-            s_win[n] = (int32_t)x;
-            if (cta == 0 && !*s_abort) P.tokens[(int64_t)n * gamma + t] = (int32_t)x;
+        }
+        __syncwarp();
+        bool late = *s_abort != 0;
+        for (int n = 0; n < B && !late; ++n) {
+          // all of this lane's slots (CTAs lane, lane + 32, ...) are requested at once; only words that do not
+          // carry this step's tag yet are read again
+          constexpr int kSlotsPerLane = kMaxGrid / 32;
+          unsigned long long w[kSlotsPerLane];
+#pragma unroll
+          for (int i = 0; i < kSlotsPerLane; ++i) {
+            const int cc = lane + 32 * i;
+            w[i] = tag;
+            if (cc < G)
+              asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w[i]) : "l"(sl + (int64_t)cc * B + n) : "memory");
+          }
+          unsigned long long best = 0ull;
+#pragma unroll
+          for (int i = 0; i < kSlotsPerLane; ++i) {
+            const int cc = lane + 32 * i;
+            uint32_t spins = 0;
+            while ((w[i] >> 56) != (unsigned long long)(t + 1) && !late) {
+              asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w[i]) : "l"(sl + (int64_t)cc * B + n) : "memory");
+              if ((++spins & 31u) == 0u && globaltimer_ns() - t_start > P.timeout_ns) late = true;
+            }
+            best = umax64(best, w[i] & 0x00FFFFFFFFFFFFFFull);
+          }
+          uint32_t hi = (uint32_t)(best >> 32), lo = (uint32_t)best;
+#pragma unroll
+          for (int off = 16; off >= 1; off >>= 1) {
+            const uint32_t ohi = __shfl_xor_sync(0xffffffffu, hi, off), olo = __shfl_xor_sync(0xffffffffu, lo, off);
+            const bool take = (ohi > hi) || (ohi == hi && olo > lo);
+            hi = take ? ohi : hi;
+            lo = take ? olo : lo;
+          }
+          late = __any_sync(0xffffffffu, late);
+          if (lane == 0 && !late) {
+            const int32_t x = (int32_t)(0xFFFFFFu - (lo & 0xFFFFFFu));
+            s_win[n] = x;
+            if (cta == 0) P.tokens[(int64_t)n * gamma + t] = x;
           }
         }
+        late = __any_sync(0xffffffffu, late);
+        if (late && lane == 0) {
+          atomicCAS(P.status, 0, kStatusTimeout);
+          *s_abort = 1;
+        }
+        trace_stamp(P, 2 + kTraceStampsPerStep * t + 2);
       }
       __syncthreads();
       if (*s_abort) break;

@@ -28,7 +28,7 @@ struct Plan {
 };
 
 struct Scratch {
-  unsigned long long* slots;  // [2][kMaxGamma * kMaxB]
+  unsigned long long* slots;  // [2 call parities][2 step parities][sm_count][kMaxB]
   unsigned int* cnt;          // two counters, 128 bytes apart
   float* ah;                  // [2][kMaxB][r]
   int* status;
@@ -45,6 +45,7 @@ struct whead_s {
   CUtensorMap tmap{};     // W: 64 x 16 boxes
   CUtensorMap tmap128{};  // W: 64 x 128 boxes
   int sm_count = 0, smem_optin = 0;
+  int64_t slots_per_parity = 0;  // 2 step parities x sm_count x kMaxB words
   Plan plan[2];  // walks <= 8, walks <= 16
   void* scratch_block = nullptr;
   Scratch s{};
@@ -66,6 +67,7 @@ int kb_of(int r) { return r / 64; }
 // SM sub-partitions (warp % 4), which each own one tensor core and one quarter of tensor memory.
 Plan make_plan(int64_t V, int r, int kind, int Bcap, int NH, int sm_count, int smem_optin, int grid_req) {
   Plan P;
+  sm_count = std::min(sm_count, kMaxGrid);
   const int KB = kb_of(r);
   const int64_t ngt = (V + kGroupRows - 1) / kGroupRows;
   const int64_t group_bytes = (int64_t)KB * kBoxBytes;
@@ -279,6 +281,8 @@ int whead_create(const void* W, const void* E, const whead_params* params, whead
   if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->device) != cudaSuccess || !coop)
     return fail(WHEAD_ERR_NO_COOP);
 
+  h->slots_per_parity = 2 * (int64_t)h->sm_count * kMaxB;
+
   // placements: walks <= 8 (one n8 half) and, if asked for, walks <= 16
   h->plan[0] = make_plan(p.V, p.r, p.kind, std::min(p.max_B, 8), 1, h->sm_count, h->smem_optin, p.grid);
   if (!h->plan[0].ok) return fail(WHEAD_ERR_UNSUPPORTED);
@@ -291,8 +295,8 @@ int whead_create(const void* W, const void* E, const whead_params* params, whead
   if (encode_w(&h->tmap, W, p.V, p.r, kGroupRows) != WHEAD_OK) return fail(WHEAD_ERR_CUDA);
   if (encode_w(&h->tmap128, W, p.V, p.r, kGroupRows * kTmaChunkGroups) != WHEAD_OK) return fail(WHEAD_ERR_CUDA);
 
-  // scratch: exchange slots (two parities), two counters on their own lines, A h slices, status word
-  const size_t slots_bytes = 2 * (size_t)kMaxGamma * kMaxB * 8;
+  // scratch: exchange slots (two call parities), two counters on their own lines, A h slices, status word
+  const size_t slots_bytes = 2 * (size_t)h->slots_per_parity * 8;
   const size_t cnt_bytes = 256;
   const size_t ah_bytes = 2 * (size_t)kMaxB * p.r * 4;
   const size_t total = slots_bytes + cnt_bytes + ah_bytes + 256;
@@ -329,9 +333,10 @@ int whead_walk_ex(whead_t* h, const float* base, const float* s0, int32_t B, int
   a.logits = out_logits;
   a.state = out_state;
   const uint32_t par = h->parity & 1u;
-  a.slots = h->s.slots + (size_t)par * kMaxGamma * kMaxB;
+  a.slots = h->s.slots + (size_t)par * h->slots_per_parity;
   a.cnt = h->s.cnt + par * 32;
-  a.slots_reset = h->s.slots + (size_t)(par ^ 1u) * kMaxGamma * kMaxB;
+  a.slots_reset = h->s.slots + (size_t)(par ^ 1u) * h->slots_per_parity;
+  a.slots_reset_count = (int32_t)h->slots_per_parity;
   a.cnt_reset = h->s.cnt + (par ^ 1u) * 32;
   a.ah = h->s.ah;
   a.status = h->s.status;
@@ -459,12 +464,13 @@ int whead_destroy(whead_t* h) {
 // ------------------------------------------------------------------------------------------------
 namespace {
 
-// Layout of the array: [slots 8 KB | counter 128 B | status 128 B] (cleared every call) then
-// [slots of the other parity 8 KB | its counter 128 B] (cleared by the kernel) then [A h slices].
-constexpr size_t kNaSlots = (size_t)kMaxGamma * kMaxB * 8;
-constexpr size_t kNaZeroBytes = kNaSlots + 256;
-constexpr size_t kNaOtherOff = kNaZeroBytes;
-constexpr size_t kNaAhOff = kNaOtherOff + kNaSlots + 128;
+// Layout of the array: [slots: 2 step parities x up to 256 CTAs x 16 walks, 64 KB][counter 128 B][status 128 B]
+// [A h slices 32 KB]. Slots, counter and status are cleared by the host before every call.
+constexpr int kNaMaxGrid = kMaxGrid;
+constexpr size_t kNaSlots = 2 * (size_t)kNaMaxGrid * kMaxB * 8;
+constexpr size_t kNaCntOff = kNaSlots;
+constexpr size_t kNaStatusOff = kNaCntOff + 128;
+constexpr size_t kNaAhOff = kNaStatusOff + 128;
 static_assert(kNaAhOff + 2 * (size_t)kMaxB * 256 * 4 <= WHEAD_NOALLOC_SCRATCH_BYTES, "scratch array too small");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[WHEAD_NOALLOC_SCRATCH_BYTES];
@@ -565,6 +571,7 @@ extern "C" int whead_walk_noalloc(const void* W, const void* E, const whead_para
   const int NH = B <= 8 ? 1 : 2;
   const Plan pl = make_plan(p.V, p.r, p.kind, B, NH, nd->sm_count, nd->smem_optin, 0);
   if (!pl.ok) return WHEAD_ERR_UNSUPPORTED;
+  if (pl.G > kNaMaxGrid) return WHEAD_ERR_UNSUPPORTED;  // more CTAs than the array has slots for
 
   CUtensorMap tmap, tmap128;
   if (encode_w(&tmap, W, p.V, p.r, kGroupRows) != WHEAD_OK) return WHEAD_ERR_CUDA;
@@ -572,7 +579,8 @@ extern "C" int whead_walk_noalloc(const void* W, const void* E, const whead_para
 
   cudaStream_t stream = static_cast<cudaStream_t>(p.stream);
   uint8_t* sc = static_cast<uint8_t*>(nd->scratch);
-  if (cudaMemsetAsync(sc, 0, kNaZeroBytes, stream) != cudaSuccess) return WHEAD_ERR_CUDA;
+  if (cudaMemsetAsync(sc, 0, 2 * (size_t)pl.G * B * 8, stream) != cudaSuccess) return WHEAD_ERR_CUDA;
+  if (cudaMemsetAsync(sc + kNaCntOff, 0, 256, stream) != cudaSuccess) return WHEAD_ERR_CUDA;
   if (out_status && cudaMemsetAsync(out_status, 0, sizeof(int32_t), stream) != cudaSuccess) return WHEAD_ERR_CUDA;
 
   WalkArgs a;
@@ -587,11 +595,11 @@ extern "C" int whead_walk_noalloc(const void* W, const void* E, const whead_para
   a.logits = out_logits;
   a.state = nullptr;
   a.slots = reinterpret_cast<unsigned long long*>(sc);
-  a.cnt = reinterpret_cast<unsigned int*>(sc + kNaSlots);
-  a.slots_reset = reinterpret_cast<unsigned long long*>(sc + kNaOtherOff);
-  a.cnt_reset = reinterpret_cast<unsigned int*>(sc + kNaOtherOff + kNaSlots);
+  a.cnt = reinterpret_cast<unsigned int*>(sc + kNaCntOff);
+  a.slots_reset = nullptr;  // cleared above by the host
+  a.cnt_reset = nullptr;
   a.ah = reinterpret_cast<float*>(sc + kNaAhOff);
-  a.status = out_status ? reinterpret_cast<int*>(out_status) : reinterpret_cast<int*>(sc + kNaSlots + 128);
+  a.status = out_status ? reinterpret_cast<int*>(out_status) : reinterpret_cast<int*>(sc + kNaStatusOff);
   a.V = p.V;
   a.t0 = 0;
   a.seed = seed;
