@@ -87,7 +87,8 @@ struct WalkArgs {
   int32_t ng;        // groups per CTA
   int32_t n_smem;    // local groups [0, n_smem) live in shared memory
   int32_t n_tmem;    // [n_smem, n_smem + n_tmem) in tensor memory
-  int32_t n_rf;      // the rest in registers (at most one per warp)
+  int32_t n_rf;      // then in registers (at most one per warp)
+  int32_t n_stream;  // the rest are re-read from global memory (L2) every step
   uint32_t tmem_cols;
   int32_t smem_w_bytes;
   int32_t ra;        // recurrent: rows of A per CTA
@@ -97,7 +98,7 @@ struct WalkArgs {
   uint32_t wl[kWarps][kMaxWarpGroups];
 };
 
-constexpr uint32_t kTierSmem = 0, kTierTmem = 1, kTierRf = 2;
+constexpr uint32_t kTierSmem = 0, kTierTmem = 1, kTierRf = 2, kTierStream = 3;
 __host__ __device__ constexpr uint32_t wl_entry(int j, uint32_t tier, int col) {
   return (uint32_t)j | (tier << 8) | ((uint32_t)col << 16);
 }
@@ -349,6 +350,27 @@ __device__ __forceinline__ void load_box_global(uint32_t (&a)[16], const uint16_
   }
 }
 
+// Box bx of a group read from global memory straight into fragment order (rows >= V read as zero).
+__device__ __forceinline__ void load_box_global_frag(uint32_t (&q)[16], const uint16_t* W, int64_t v0, int64_t V, int r,
+                                                     int bx, int c) {
+  uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0, y0 = x0, y1 = x0;
+  if (v0 < V) {
+    const uint4* p = reinterpret_cast<const uint4*>(W + v0 * r + 64 * bx + 16 * c);
+    x0 = __ldg(p);
+    x1 = __ldg(p + 1);
+  }
+  if (v0 + 8 < V) {
+    const uint4* p = reinterpret_cast<const uint4*>(W + (v0 + 8) * r + 64 * bx + 16 * c);
+    y0 = __ldg(p);
+    y1 = __ldg(p + 1);
+  }
+  // x: row g chunks 2c (x0) and 2c + 1 (x1); y: row g + 8. Op m = 2 rho + h takes {R[2h], S[2h], R[2h+1], S[2h+1]}.
+  q[0] = x0.x; q[1] = y0.x; q[2] = x0.y; q[3] = y0.y;
+  q[4] = x0.z; q[5] = y0.z; q[6] = x0.w; q[7] = y0.w;
+  q[8] = x1.x; q[9] = y1.x; q[10] = x1.y; q[11] = y1.y;
+  q[12] = x1.z; q[13] = y1.z; q[14] = x1.w; q[15] = y1.w;
+}
+
 // Builds the B fragments of walk n from an fp32 state row (global or shared), rounding to bf16.
 template <int KB>
 __device__ __forceinline__ void bfrag_from_f32(uint32_t (&bf)[KB][8], const float* s, int c) {
@@ -507,6 +529,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+  // streamed groups: ask L2 for their rows now, so that every step reads them from L2
+  for (int e = 0; e < my_count; ++e) {
+    const uint32_t ent = __shfl_sync(0xffffffffu, my_entry, e);
+    if (((ent >> 8) & 3u) != kTierStream) continue;
+    // the group's 16 rows are 32 r contiguous bytes: one prefetch per 128-byte line, rows below V only
+    const int64_t v0 = row_base + (int64_t)kGroupRows * (int)(ent & 0xFFu);
+    const uint8_t* gb = reinterpret_cast<const uint8_t*>(P.W + v0 * r);
+    for (int L = lane; L < r / 4; L += 32)
+      if (v0 + (L * 128) / (2 * r) < V) prefetch_l2(gb + L * 128);
+  }
 
   // recurrent head: the initial state and this CTA's rows of A
   const int a_lo = cta * P.ra;
@@ -665,6 +697,19 @@ __global__ void __launch_bounds__(kThreads, 1)
               for (int h = 0; h < NH; ++h)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) acc[s][h][q] = 0.f;
+          }
+        } else if (tier == kTierStream) {
+          // boxes in flight per batch: all of them when registers allow (one batch half, no register group),
+          // two with both batch halves live, one in warps that also hold a register-resident group
+          const int64_t v0 = row_base + (int64_t)kGroupRows * j + g;
+          constexpr int SB = RFW ? 1 : ((NH == 1 || KB < 4) ? KB : 2);
+#pragma unroll
+          for (int b0 = 0; b0 < KB; b0 += SB) {
+            uint32_t a[SB][16];
+#pragma unroll
+            for (int i = 0; i < SB; ++i) load_box_global_frag(a[i], P.W, v0, V, r, b0 + i, c);
+#pragma unroll
+            for (int i = 0; i < SB; ++i) mma_box<KB, NH>(acc, a[i], bf, b0 + i);
           }
         } else {
           if constexpr (RFW) {

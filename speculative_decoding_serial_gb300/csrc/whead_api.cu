@@ -75,7 +75,7 @@ Plan make_plan(int64_t V, int r, int kind, int Bcap, int NH, int sm_count, int s
   const int tmem_max = 128 / KB;
   const int rf_max = (NH == 1) ? 8 : 0;  // at most two register warps per lane quadrant
 
-  auto fits = [&](int G, Plan& out) -> bool {
+  auto fits = [&](int G, Plan& out, bool allow_stream) -> bool {
     const int64_t ng64 = (ngt + G - 1) / G;
     if (ng64 > 255) return false;
     const int ng = (int)ng64;
@@ -89,13 +89,15 @@ Plan make_plan(int64_t V, int r, int kind, int Bcap, int NH, int sm_count, int s
     rem -= n_tmem;
     int n_rf = std::min(rem, rf_max);
     rem -= n_rf;
-    if (rem > 0) return false;
+    if (rem > 0 && !allow_stream) return false;
+    const int n_stream = rem;
     out = Plan();
     out.G = G;
     out.ng = ng;
     out.n_smem = n_smem;
     out.n_tmem = n_tmem;
     out.n_rf = n_rf;
+    out.n_stream = n_stream;
     out.ra = ra;
     out.Bcap = Bcap;
     out.smem_w_bytes = (int)(n_smem * group_bytes);
@@ -111,35 +113,45 @@ Plan make_plan(int64_t V, int r, int kind, int Bcap, int NH, int sm_count, int s
     const int rf_per_q = (n_rf + 3) / 4;
     const int tmem_warps_per_q = (kWarps / 4) - rf_per_q;
     if (n_tmem > 0 && tmem_warps_per_q < 1) return false;
+    // relative cost of a group by tier, measured on GB300: tensor memory 5, register 5, shared 6, streamed 9
     int load[kWarps] = {};
     int sp_load[4] = {};
-    auto push = [&](int w, uint32_t entry) -> bool {
+    auto push = [&](int w, uint32_t entry, int cost) -> bool {
       if (out.wl_count[w] >= kMaxWarpGroups) return false;
       out.wl[w][out.wl_count[w]++] = entry;
-      load[w]++;
-      sp_load[w & 3]++;
+      load[w] += cost;
+      sp_load[w & 3] += cost;
       return true;
     };
     for (int i = 0; i < n_rf; ++i) {
       const int q = i & 3, k = i >> 2;  // k-th register warp of quadrant q, counted from the top
       const int w = q + 4 * ((kWarps / 4) - 1 - k);
       out.rf_warp_mask |= 1u << w;
-      if (!push(w, wl_entry(n_smem + n_tmem + i, kTierRf, 0))) return false;
+      if (!push(w, wl_entry(n_smem + n_tmem + i, kTierRf, 0), 5)) return false;
     }
     for (int i = 0; i < n_tmem; ++i) {
       const int q = i & 3, idx = i >> 2;
       const int w = q + 4 * (idx % tmem_warps_per_q);
-      if (!push(w, wl_entry(n_smem + i, kTierTmem, idx * 16 * KB))) return false;
+      if (!push(w, wl_entry(n_smem + i, kTierTmem, idx * 16 * KB), 5)) return false;
     }
-    for (int j = 0; j < n_smem; ++j) {
-      int q = 0;
-      for (int k = 1; k < 4; ++k)
-        if (sp_load[k] < sp_load[q]) q = k;
-      int best = q;
-      for (int w = q; w < kWarps; w += 4)
-        if (load[w] < load[best]) best = w;
-      if (!push(best, wl_entry(j, kTierSmem, 0))) return false;
-    }
+    // least-loaded sub-partition, then its least-loaded eligible warp
+    auto place = [&](uint32_t entry, int cost, bool rf_ok) -> bool {
+      int bq = -1, bw = -1;
+      for (int q = 0; q < 4; ++q) {
+        int w_best = -1;
+        for (int w = q; w < kWarps; w += 4)
+          if ((rf_ok || !((out.rf_warp_mask >> w) & 1u)) && (w_best < 0 || load[w] < load[w_best])) w_best = w;
+        if (w_best >= 0 && (bq < 0 || sp_load[q] < sp_load[bq])) {
+          bq = q;
+          bw = w_best;
+        }
+      }
+      return bw >= 0 && push(bw, entry, cost);
+    };
+    for (int i = 0; i < n_stream; ++i)
+      if (!place(wl_entry(n_smem + n_tmem + n_rf + i, kTierStream, 0), 9, true)) return false;
+    for (int j = 0; j < n_smem; ++j)
+      if (!place(wl_entry(j, kTierSmem, 0), 6, true)) return false;
     out.ok = true;
     return true;
   };
@@ -147,14 +159,16 @@ Plan make_plan(int64_t V, int r, int kind, int Bcap, int NH, int sm_count, int s
   int G;
   if (grid_req > 0) {
     G = std::min(grid_req, sm_count);
-    if (!fits(G, P)) P.ok = false;
+    if (!fits(G, P, true)) P.ok = false;
     return P;
   }
-  // few CTAs for small heads (cheaper exchange), more until the shard fits on chip
+  // few CTAs for small heads (cheaper exchange), more until the shard fits on chip; if it never fits, all
+  // SMs with the overflow streamed (partial residency)
   const int64_t target = 96 * 1024;
   G = (int)std::min<int64_t>(sm_count, std::max<int64_t>(1, (ngt * group_bytes + target - 1) / target));
   for (; G <= sm_count; ++G)
-    if (fits(G, P)) return P;
+    if (fits(G, P, false)) return P;
+  if (fits(sm_count, P, true)) return P;
   P.ok = false;
   return P;
 }
@@ -358,6 +372,7 @@ int whead_walk_ex(whead_t* h, const float* base, const float* s0, int32_t B, int
   a.n_smem = pl.n_smem;
   a.n_tmem = pl.n_tmem;
   a.n_rf = pl.n_rf;
+  a.n_stream = pl.n_stream;
   a.tmem_cols = pl.tmem_cols;
   a.smem_w_bytes = pl.smem_w_bytes;
   a.ra = pl.ra;
@@ -614,6 +629,7 @@ extern "C" int whead_walk_noalloc(const void* W, const void* E, const whead_para
   a.n_smem = pl.n_smem;
   a.n_tmem = pl.n_tmem;
   a.n_rf = pl.n_rf;
+  a.n_stream = pl.n_stream;
   a.tmem_cols = pl.tmem_cols;
   a.smem_w_bytes = pl.smem_w_bytes;
   a.ra = pl.ra;

@@ -206,3 +206,49 @@ def test_phase_trace_stamps_are_ordered(torch_cuda):
     assert (clk > 0).all()
     assert (np.diff(clk, axis=1) >= 0).all()      # stamps of every CTA are in program order
     head.close()
+
+
+# --- partial residency: groups that do not fit on chip are re-read from L2 every step -------------
+STREAMED = [
+    # kind, V, r, B, gamma, T, grid (a small grid forces most groups to stream)
+    (O.MARKOV, 40000, 256, 1, 4, 0.0, 12),
+    (O.MARKOV, 30011, 128, 3, 3, 1.0, 8),
+    (O.RECURRENT, 20000, 256, 2, 3, 0.0, 6),
+    (O.MARKOV, 40000, 256, 12, 2, 0.0, 24),
+]
+
+
+@pytest.mark.parametrize("kind,V,r,B,gamma,T,grid", STREAMED)
+def test_streamed_parity(torch_cuda, kind, V, r, B, gamma, T, grid):
+    d = I.make_inputs(kind, V, r, B, gamma, seed=V + B)
+    dd = to_device(d, "cuda")
+    head = make_head(torch_cuda, d, dd, max_B=B, max_gamma=gamma, grid=grid)
+    plan = head.plan(B)
+    assert plan["stream_groups"] > 0, plan
+    check_walk(head, d, dd, T=T, seed=77)
+    head.close()
+
+
+@pytest.mark.parametrize("name", ["markov_v248064_r256_b1_g16", "markov_v248064_r256_b4_g16"])
+def test_workload_parity_partial_residency(torch_cuda, name):
+    w = I.WORKLOADS[name]
+    d = I.workload_inputs(name)
+    dd = to_device(d, "cuda")
+    head = make_head(torch_cuda, d, dd, max_B=w["B"], max_gamma=w["gamma"])
+    plan = head.plan(w["B"])
+    print(name, plan)
+    assert plan["stream_groups"] > 0
+    near = []
+    check_walk(head, d, dd, T=w["T"], seed=0, report=near)
+    print("near-tie steps:", near)
+    head.close()
+
+
+def test_sweep_point_sixteen_walks(torch_cuda):
+    """B = 16 at V = 151,936 (gamma 7, sampled): two batch halves, partially resident."""
+    d = I.make_inputs(O.MARKOV, 151936, 256, 16, 7, seed=0)
+    dd = to_device(d, "cuda")
+    head = make_head(torch_cuda, d, dd, max_B=16, max_gamma=7)
+    print(head.plan(16))
+    check_walk(head, d, dd, T=1.0, seed=11)
+    head.close()
