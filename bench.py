@@ -27,13 +27,29 @@ sys.path.insert(0, ROOT)
 METRIC = "us per gamma=16 draft walk (B=1, V=152k, greedy) & % of on-chip-BW roofline"
 DEFAULT_WORKLOAD = "markov_v151936_r256_b1_g16"
 
-# Per-SM on-chip figures used by the roofline (bytes per SM clock). Shared memory: 32 banks x 4 B.
-# Tensor memory read by tcgen05.ld: measured on GB300 with an in-bounds probe (32x32b.x64, 512 threads).
+# Per-SM on-chip figures for the roofline (bytes per SM clock), measured live by the probe library when it
+# loads; these are the fallbacks (shared memory: 32 banks x 4 B; tensor memory: tcgen05.ld measured on GB300).
 SMEM_B_PER_CLK = 128.0
 TMEM_B_PER_CLK = 428.0
 TMEM_BYTES = 128 * 512 * 4
 # Registers this kernel family can dedicate to W: one 16-row group per warp, 12 warps.
 RF_W_BYTES_CAP = 12 * 16 * 512
+
+
+def probe_onchip():
+    """Shared/tensor-memory bytes per SM clock, mma.sync clocks per op and grid-exchange clocks (measured)."""
+    import ctypes
+    from speculative_decoding_serial_gb300 import build
+    try:
+        L = ctypes.CDLL(build.PROBE_LIB)
+        out = (ctypes.c_double * 4)()
+        rc = L.whead_probe_onchip(out)
+        if rc != 0:
+            return None
+        return {"smem_b_per_clk": out[0], "tmem_b_per_clk": out[1], "mma_m16n8k16_clk_per_sm": out[2],
+                "grid_exchange_clk": out[3]}
+    except OSError:
+        return None
 
 
 def load_peaks():
@@ -292,12 +308,15 @@ def ours(args, world, rank, local):
 
     # roofline (on-chip operand bandwidth for the steps, HBM for the one-time shard load)
     hbm_gbs, peak_kind = load_peaks()
+    onchip = probe_onchip()
+    smem_bpc = onchip["smem_b_per_clk"] if onchip else SMEM_B_PER_CLK
+    tmem_bpc = onchip["tmem_b_per_clk"] if onchip else TMEM_B_PER_CLK
     sm = plan["sm_count"]
     wbytes = V * r * 2
     w_per_sm = plan["groups_per_cta"] * 16 * r * 2
     smem_min = max(0, w_per_sm - TMEM_BYTES - RF_W_BYTES_CAP)
     tmem_used = min(TMEM_BYTES, w_per_sm)
-    t_star_clk = max(smem_min / SMEM_B_PER_CLK, tmem_used / TMEM_B_PER_CLK)
+    t_star_clk = max(smem_min / smem_bpc, tmem_used / tmem_bpc)
     mhz = clocks["sm_mhz"] or 1447.0
     t_star_us = t_star_clk / mhz
     t_entry_us = wbytes / (hbm_gbs * 1e3)
@@ -344,7 +363,9 @@ def ours(args, world, rank, local):
         "roofline": {"bound": "onchip", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": t_roof_us / us_per_walk, "traffic": None,
                      "t_roof_us": t_roof_us, "t_entry_us": t_entry_us, "t_star_clk_per_step": t_star_clk,
-                     "hbm_peak_gbs": hbm_gbs, "hbm_peak_kind": peak_kind, "clock_mhz": mhz},
+                     "hbm_peak_gbs": hbm_gbs, "hbm_peak_kind": peak_kind, "clock_mhz": mhz,
+                     "onchip_measured": onchip,
+                     "onchip_kind": "measured" if onchip else "fallback (128 B/clk shared, 428 B/clk tensor memory)"},
         "per_step": {"slope_us": slope, "intercept_us": intercept, "gammas": fit_g, "median_us": fit_t,
                      "t_star_us": t_star_us,
                      "frac_of_onchip_roofline": (t_star_us / slope) if slope else None},

@@ -1,0 +1,188 @@
+// onchip_probe.cu — measures the per-SM figures the walk's on-chip roofline is expressed in.
+//
+// Built as a separate library (libwhead_probe.so) for the benchmark; the walk library does not use it.
+//   whead_probe_onchip(out[4]):
+//     out[0] shared-memory read bandwidth, bytes per SM clock (ld.shared.v4, 384 threads, 192 KB resident)
+//     out[1] tensor-memory read bandwidth, bytes per SM clock (tcgen05.ld.32x32b.x32, 384 threads, 512 cols)
+//     out[2] SM clocks per mma.sync.m16n8k16 bf16 -> fp32 per SM (independent accumulators, 384 threads)
+//     out[3] SM clocks per grid-wide arrival + wait over all SMs (relaxed counter; cooperative launch)
+// Every wait is bounded; every access stays inside its buffer. Returns 0, or a negative CUDA error.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <vector>
+
+namespace {
+
+constexpr int kThreads = 384;
+
+__global__ void __launch_bounds__(kThreads, 1) smem_bw(uint32_t* out, long long* cyc, int iters, int bytes) {
+  extern __shared__ __align__(16) uint8_t sm[];
+  uint32_t* s = reinterpret_cast<uint32_t*>(sm);
+  for (int i = threadIdx.x; i < bytes / 4; i += blockDim.x) s[i] = i * 2654435761u;
+  __syncthreads();
+  uint32_t a0 = 0, a1 = 0, a2 = 0, a3 = 0;
+  const int n16 = bytes / 16;
+  const long long t0 = clock64();
+  for (int it = 0; it < iters; ++it) {
+#pragma unroll 4
+    for (int i = threadIdx.x; i < n16; i += blockDim.x) {
+      const uint4 v = reinterpret_cast<const uint4*>(sm)[i];
+      a0 ^= v.x; a1 ^= v.y; a2 ^= v.z; a3 ^= v.w;
+    }
+  }
+  __syncthreads();
+  const long long t1 = clock64();
+  out[blockIdx.x * blockDim.x + threadIdx.x] = a0 ^ a1 ^ a2 ^ a3;
+  if (threadIdx.x == 0) cyc[blockIdx.x] = t1 - t0;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) tmem_bw(uint32_t* out, long long* cyc, int iters) {
+  __shared__ uint32_t taddr_s;
+  const int warp = threadIdx.x >> 5;
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+        (uint32_t)__cvta_generic_to_shared(&taddr_s)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;");
+  const uint32_t taddr = taddr_s;
+  const int quad = warp & 3, grp = warp >> 2, ngrp = (blockDim.x >> 5) >> 2;
+  const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+  uint32_t acc = 0;
+  const long long t0 = clock64();
+  for (int it = 0; it < iters; ++it) {
+    for (int col = grp * 32; col < 512; col += ngrp * 32) {
+      uint32_t r[32];
+      asm volatile(
+          "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+          "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+          : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+            "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+            "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+            "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+          : "r"(taddr + lane_base + (uint32_t)col));
+      asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+      for (int j = 0; j < 32; ++j) acc ^= r[j];
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;");
+  __syncthreads();
+  const long long t1 = clock64();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(taddr));
+  out[blockIdx.x * blockDim.x + threadIdx.x] = acc;
+  if (threadIdx.x == 0) cyc[blockIdx.x] = t1 - t0;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) mma_rate(float* out, long long* cyc, int iters) {
+  const uint32_t a0 = threadIdx.x, a1 = threadIdx.x * 3u, a2 = threadIdx.x * 5u, a3 = threadIdx.x * 7u;
+  const uint32_t b0 = 0x3f803f80u, b1 = 0x3f803f80u;
+  float c[8][4];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.f;
+  const long long t0 = clock64();
+  for (int it = 0; it < iters; ++it) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      asm volatile(
+          "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+          : "+f"(c[j][0]), "+f"(c[j][1]), "+f"(c[j][2]), "+f"(c[j][3])
+          : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+  __syncthreads();
+  const long long t1 = clock64();
+  float s = 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) s += c[j][0] + c[j][1] + c[j][2] + c[j][3];
+  out[blockIdx.x * blockDim.x + threadIdx.x] = s;
+  if (threadIdx.x == 0) cyc[blockIdx.x] = t1 - t0;
+}
+
+__global__ void __launch_bounds__(kThreads, 1) grid_exchange(unsigned int* counter, int* status, long long* cyc,
+                                                             int iters) {
+  const unsigned int G = gridDim.x;
+  __syncthreads();
+  const long long t0 = clock64();
+  for (int it = 0; it < iters; ++it) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(counter) : "memory");
+      const unsigned int target = (unsigned int)(it + 1) * G;
+      uint32_t spins = 0;
+      while (true) {
+        unsigned int v;
+        asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+        if (v >= target) break;
+        if (++spins > 4000000u) {
+          atomicExch(status, 1);
+          break;
+        }
+      }
+    }
+    __syncthreads();
+  }
+  const long long t1 = clock64();
+  if (threadIdx.x == 0) cyc[blockIdx.x] = t1 - t0;
+}
+
+double median_cycles(const long long* d_cyc, int n) {
+  std::vector<long long> h(n);
+  if (cudaMemcpy(h.data(), d_cyc, n * sizeof(long long), cudaMemcpyDeviceToHost) != cudaSuccess) return -1.0;
+  std::sort(h.begin(), h.end());
+  return (double)h[n / 2];
+}
+
+}  // namespace
+
+extern "C" int whead_probe_onchip(double* out) {
+  int dev = 0, nsm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  uint32_t* d_out = nullptr;
+  long long* d_cyc = nullptr;
+  unsigned int* d_cnt = nullptr;
+  int* d_status = nullptr;
+  int rc = 0;
+  const int smem_bytes = 192 * 1024;
+  do {
+    if (cudaMalloc(&d_out, (size_t)nsm * kThreads * 4) != cudaSuccess) { rc = -2; break; }
+    if (cudaMalloc(&d_cyc, (size_t)nsm * 8) != cudaSuccess) { rc = -2; break; }
+    if (cudaMalloc(&d_cnt, 256) != cudaSuccess) { rc = -2; break; }
+    if (cudaMalloc(&d_status, 4) != cudaSuccess) { rc = -2; break; }
+    if (cudaFuncSetAttribute(smem_bw, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess) { rc = -3; break; }
+    if (cudaFuncSetAttribute(tmem_bw, cudaFuncAttributeMaxDynamicSharedMemorySize, 160 * 1024) != cudaSuccess) { rc = -3; break; }
+    const int it_smem = 200;
+    smem_bw<<<nsm, kThreads, smem_bytes>>>(d_out, d_cyc, 2, smem_bytes);
+    smem_bw<<<nsm, kThreads, smem_bytes>>>(d_out, d_cyc, it_smem, smem_bytes);
+    if (cudaDeviceSynchronize() != cudaSuccess) { rc = -4; break; }
+    out[0] = (double)smem_bytes * it_smem / median_cycles(d_cyc, nsm);
+    // 160 KB of dynamic shared memory keeps one CTA per SM, so every CTA owns all 512 columns
+    const int it_tmem = 200;
+    tmem_bw<<<nsm, kThreads, 160 * 1024>>>(d_out, d_cyc, 2);
+    tmem_bw<<<nsm, kThreads, 160 * 1024>>>(d_out, d_cyc, it_tmem);
+    if (cudaDeviceSynchronize() != cudaSuccess) { rc = -4; break; }
+    out[1] = (double)it_tmem * 512 * 128 * 4 / median_cycles(d_cyc, nsm);
+    const int it_mma = 2000;
+    mma_rate<<<nsm, kThreads>>>(reinterpret_cast<float*>(d_out), d_cyc, 10);
+    mma_rate<<<nsm, kThreads>>>(reinterpret_cast<float*>(d_out), d_cyc, it_mma);
+    if (cudaDeviceSynchronize() != cudaSuccess) { rc = -4; break; }
+    out[2] = median_cycles(d_cyc, nsm) / ((double)it_mma * 8 * (kThreads / 32));
+    int iters = 1000;
+    if (cudaMemset(d_cnt, 0, 256) != cudaSuccess || cudaMemset(d_status, 0, 4) != cudaSuccess) { rc = -4; break; }
+    void* args[] = {&d_cnt, &d_status, &d_cyc, &iters};
+    if (cudaLaunchCooperativeKernel((const void*)grid_exchange, nsm, kThreads, args, 0, 0) != cudaSuccess) { rc = -5; break; }
+    if (cudaDeviceSynchronize() != cudaSuccess) { rc = -4; break; }
+    int st = 0;
+    cudaMemcpy(&st, d_status, 4, cudaMemcpyDeviceToHost);
+    out[3] = st ? -1.0 : median_cycles(d_cyc, nsm) / iters;
+  } while (false);
+  if (d_out) cudaFree(d_out);
+  if (d_cyc) cudaFree(d_cyc);
+  if (d_cnt) cudaFree(d_cnt);
+  if (d_status) cudaFree(d_status);
+  return rc;
+}
