@@ -36,6 +36,23 @@ TMEM_BYTES = 128 * 512 * 4
 RF_W_BYTES_CAP = 12 * 16 * 512
 
 
+def recorded_traffic():
+    """DRAM bytes per walk launch from the committed ncu summary, if it was taken on the current kernel source."""
+    import hashlib
+    import re
+    src = os.path.join(ROOT, "speculative_decoding_serial_gb300", "csrc", "walk_kernel.cuh")
+    prof = os.path.join(ROOT, "profiles", "walk_kernel_markov_v151936_r256_b1_g16.md")
+    try:
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        m = re.search(r"traffic_bytes_per_launch: (\d+) \(walk_kernel.cuh sha256 prefix ([0-9a-f]+)\)",
+                      open(prof).read())
+        if m and m.group(2) == h:
+            return int(m.group(1))
+    except OSError:
+        pass
+    return None
+
+
 def probe_onchip():
     """Shared/tensor-memory bytes per SM clock, mma.sync clocks per op and grid-exchange clocks (measured)."""
     import ctypes
@@ -361,7 +378,8 @@ def ours(args, world, rank, local):
         "config": {"workload": args.workload, "V": V, "r": r, "B": B, "gamma": gamma, "T": w["T"],
                    "l2": "flushed (256 MB write) before every timed walk", "placement": plan},
         "roofline": {"bound": "onchip", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": t_roof_us / us_per_walk, "traffic": None,
+                     "frac": t_roof_us / us_per_walk,
+                     "traffic": recorded_traffic() if args.workload == DEFAULT_WORKLOAD else None,
                      "t_roof_us": t_roof_us, "t_entry_us": t_entry_us, "t_star_clk_per_step": t_star_clk,
                      "hbm_peak_gbs": hbm_gbs, "hbm_peak_kind": peak_kind, "clock_mhz": mhz,
                      "onchip_measured": onchip,
