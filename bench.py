@@ -397,6 +397,64 @@ def ours(args, world, rank, local):
     print(json.dumps(line))
 
 
+def sweep(args):
+    """Latency of every workload of the pages (one JSON line each): the small case, the B x gamma x T sweep at
+    V = 151,936, partial residency at V = 248,064 and the recurrent head. Not part of the default run."""
+    import numpy as np
+    import torch
+
+    import whead_inputs as I
+    from speculative_decoding_serial_gb300 import build
+    from speculative_decoding_serial_gb300 import whead as wh
+
+    build.build()
+    dev = torch.device("cuda", 0)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    cases = []
+    for name in ("markov_v4096_r64_b1_g4", "markov_v248064_r256_b1_g16", "markov_v248064_r256_b4_g16",
+                 "recurrent_v151936_r256_b1_g15"):
+        w = I.WORKLOADS[name]
+        cases.append((name, w["kind"], w["V"], w["r"], w["B"], w["gamma"], w["T"]))
+    sw = I.SWEEP
+    for B in sw["Bs"]:
+        for g in sw["gammas"]:
+            for T in sw["Ts"]:
+                cases.append((f"sweep_v{sw['V']}_b{B}_g{g}_t{int(T)}", sw["kind"], sw["V"], sw["r"], B, g, T))
+    cache = {}
+    for name, kind, V, r, B, g, T in cases:
+        key = (kind, V, r, B, g)
+        if key not in cache:
+            cache.clear()
+            d = I.make_inputs(kind, V, r, B, g, seed=0)
+            cache[key] = d
+        d = cache[key]
+        W = torch.from_numpy(d["W"].view(np.int16)).view(torch.bfloat16).to(dev)
+        E = torch.from_numpy(d["E"].view(np.int16)).view(torch.bfloat16).to(dev)
+        base = torch.from_numpy(d["base"]).to(dev)
+        s0 = torch.from_numpy(d["s0"]).to(dev)
+        A = None if d["A"] is None else torch.from_numpy(d["A"]).to(dev)
+        c = None if d["c"] is None else torch.from_numpy(d["c"]).to(dev)
+        head = wh.Head(W, E, kind=kind, A=A, c=c, max_B=B, max_gamma=g, stream=stream)
+        tok = torch.empty((B, g), dtype=torch.int32, device=dev)
+        for _ in range(5):
+            head.walk(base, s0, T=T, out_tokens=tok)
+        ts = []
+        for _ in range(args.sweep_walks):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            head.walk(base, s0, T=T, out_tokens=tok)
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        st = head.status()
+        print(json.dumps({"case": name, "kind": "recurrent" if kind else "markov", "V": V, "r": r, "B": B,
+                          "gamma": g, "T": T, "us_per_walk": statistics.median(ts), "status": st,
+                          "placement": head.plan(B)}), flush=True)
+        head.close()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -406,7 +464,12 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--sweep", action="store_true", help="latency of every workload of the pages (one line each)")
+    ap.add_argument("--sweep-walks", type=int, default=100)
     args = ap.parse_args()
+    if args.sweep:
+        sweep(args)
+        return
     args.warmup = max(3, args.warmup)
     world, rank, local = dist_setup(args)
     if args.impl == "reference":
