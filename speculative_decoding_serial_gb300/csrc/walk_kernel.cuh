@@ -631,8 +631,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tau = (uint32_t)(P.t0 + t);
       trace_stamp(P, 2 + kTraceStampsPerStep * t);
 
-      // recurrent: this CTA's slice of A h_t, published with the step's arrival
-      if (recurrent && warp == 0) {
+      // recurrent: this CTA's slice of A h_t, published with the step's arrival (warp 0, never a register warp,
+      // so the register warps' copy of the loop does not carry this code)
+      if (!RFW && recurrent && warp == 0) {
         for (int p = 0; p < B * P.ra; ++p) {
           const int n = p / P.ra, i = p % P.ra;
           if (a_lo + i >= r) continue;
@@ -816,7 +817,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // step's. No fence is needed because the answer is taken only from words that carry this step's tag.
       // Slots alternate between two step buffers: a CTA can reach step t + 2 only after every CTA has
       // arrived at step t + 1, that is, after every CTA has finished reading step t's buffer.
-      if (warp == 0) {
+      if (!RFW && warp == 0) {
         unsigned long long kk = 0ull;
         if (lane < B)
           for (int w = 0; w < kWarps; ++w) kk = umax64(kk, s_red[w * kMaxB + lane]);

@@ -125,7 +125,7 @@ Plan make_plan(int64_t V, int r, int kind, int Bcap, int NH, int sm_count, int s
     };
     for (int i = 0; i < n_rf; ++i) {
       const int q = i & 3, k = i >> 2;  // k-th register warp of quadrant q, counted from the top
-      const int w = q + 4 * ((kWarps / 4) - 1 - k);
+      const int w = q + 4 * ((kWarps / 4) - 1 - k);  // never warp 0: it runs the exchange
       out.rf_warp_mask |= 1u << w;
       if (!push(w, wl_entry(n_smem + n_tmem + i, kTierRf, 0), 5)) return false;
     }
