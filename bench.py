@@ -455,6 +455,86 @@ def sweep(args):
         head.close()
 
 
+def ablation(args):
+    """Fusion versus residency on GB300 (Figs. 4 and 11 of the pages): complete-call latency over gamma in
+    {1, 7, 16} and its least-squares slope (us/step) and intercept (entry) for (a) the resident megakernel,
+    (b) the same fused walk with every row of W re-read from L2/HBM each step, and (c) step-wise execution,
+    one launch per step (each launch loads W again). One JSON line per variant."""
+    import numpy as np
+    import torch
+
+    import whead_inputs as I
+    from speculative_decoding_serial_gb300 import build
+    from speculative_decoding_serial_gb300 import whead as wh
+
+    build.build()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    w = I.WORKLOADS[args.workload]
+    d = I.workload_inputs(args.workload)
+    B, G16, V, r = w["B"], w["gamma"], w["V"], w["r"]
+    W = torch.from_numpy(d["W"].view(np.int16)).view(torch.bfloat16).to(dev)
+    E = torch.from_numpy(d["E"].view(np.int16)).view(torch.bfloat16).to(dev)
+    base = torch.from_numpy(d["base"]).to(dev)
+    s0 = torch.from_numpy(d["s0"]).to(dev)
+    A = None if d["A"] is None else torch.from_numpy(d["A"]).to(dev)
+    c = None if d["c"] is None else torch.from_numpy(d["c"]).to(dev)
+    gammas = [g for g in (1, 7, 16) if g <= G16]
+
+    def timed(fn, n):
+        for _ in range(3):
+            fn()
+        ts = []
+        for _ in range(n):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1) * 1e3)
+        return statistics.median(ts)
+
+    def fit(xs, ys):
+        xm, ym = sum(xs) / len(xs), sum(ys) / len(ys)
+        sl = sum((a - xm) * (b - ym) for a, b in zip(xs, ys)) / sum((a - xm) ** 2 for a in xs)
+        return sl, ym - sl * xm
+
+    variants = {}
+    for name, flags in (("resident", 0), ("fused_streaming", wh.FLAG_FORCE_STREAM)):
+        head = wh.Head(W, E, kind=w["kind"], A=A, c=c, max_B=B, max_gamma=G16, stream=stream, flags=flags)
+        plan = head.plan(B)
+        ys = []
+        for g in gammas:
+            bg = base[:, :g].contiguous()
+            tok = torch.empty((B, g), dtype=torch.int32, device=dev)
+            ys.append(timed(lambda: head.walk(bg, s0, T=w["T"], out_tokens=tok), args.sweep_walks))
+        assert head.status() == 0
+        head.close()
+        variants[name] = (ys, plan)
+    # step-wise: one launch per step, the state handed over through device memory
+    head = wh.Head(W, E, kind=w["kind"], A=A, c=c, max_B=B, max_gamma=1, stream=stream)
+    steps_base = [base[:, t:t + 1].contiguous() for t in range(G16)]
+    st = torch.empty((G16 + 1, B, r), dtype=torch.float32, device=dev)
+    tok1 = torch.empty((B, 1), dtype=torch.int32, device=dev)
+    ys = []
+    for g in gammas:
+        def stepwise(g=g):
+            cur = s0
+            for t in range(g):
+                head.walk_ex(steps_base[t], cur, T=w["T"], t0=t, out_tokens=tok1, out_state=st[t + 1])
+                cur = st[t + 1]
+        ys.append(timed(stepwise, max(10, args.sweep_walks // 4)))
+    assert head.status() == 0
+    variants["step_wise"] = (ys, head.plan(B))
+    head.close()
+    for name, (ys, plan) in variants.items():
+        sl, ic = fit(gammas, ys)
+        print(json.dumps({"ablation": name, "workload": args.workload, "gammas": gammas, "us_per_walk": ys,
+                          "us_per_step_slope": sl, "entry_intercept_us": ic, "placement": plan}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -466,9 +546,13 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--sweep", action="store_true", help="latency of every workload of the pages (one line each)")
     ap.add_argument("--sweep-walks", type=int, default=100)
+    ap.add_argument("--ablation", action="store_true", help="fusion vs residency (resident / fused streaming / step-wise)")
     args = ap.parse_args()
     if args.sweep:
         sweep(args)
+        return
+    if args.ablation:
+        ablation(args)
         return
     args.warmup = max(3, args.warmup)
     world, rank, local = dist_setup(args)

@@ -49,6 +49,8 @@ typedef enum { WHEAD_MARKOV = 0, WHEAD_RECURRENT = 1 } whead_kind;
 /* Flags (whead_params.flags). */
 #define WHEAD_FLAG_LOGITS_F32 (1u << 0)      /* out_logits holds fp32 z instead of bf16(z) */
 #define WHEAD_FLAG_FIXED_LATENT (1u << 1)    /* measurement mode: never advance the state (Fig. 13b probe) */
+#define WHEAD_FLAG_FORCE_STREAM (1u << 2)    /* measurement mode: keep no row of W on chip; every step re-reads all
+                                                of W from L2/HBM (the fused but non-resident walk of Figs. 4, 11) */
 #define WHEAD_FLAG_FAULT_SKIP_ARRIVAL (1u << 8) /* testing: CTA 0 never arrives at step 0's exchange, so
                                                    every other CTA's bounded wait runs out */
 

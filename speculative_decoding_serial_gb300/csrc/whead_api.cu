@@ -65,7 +65,8 @@ int kb_of(int r) { return r / 64; }
 
 // Planner: number of CTAs, groups per CTA and their tier; per-warp work lists balanced over the four
 // SM sub-partitions (warp % 4), which each own one tensor core and one quarter of tensor memory.
-Plan make_plan(int64_t V, int r, int kind, int Bcap, int NH, int sm_count, int smem_optin, int grid_req) {
+Plan make_plan(int64_t V, int r, int kind, int Bcap, int NH, int sm_count, int smem_optin, int grid_req,
+               bool force_stream = false) {
   Plan P;
   sm_count = std::min(sm_count, kMaxGrid);
   const int KB = kb_of(r);
@@ -82,12 +83,12 @@ Plan make_plan(int64_t V, int r, int kind, int Bcap, int NH, int sm_count, int s
     const int ra = recurrent ? (r + G - 1) / G : 0;
     const SmemLayout L0 = SmemLayout::make(0, Bcap, r, ra, recurrent, ng);
     const int64_t fixed = 1024 + L0.total;
-    const int64_t smem_groups_max = std::max<int64_t>(0, (smem_optin - fixed) / group_bytes);
+    const int64_t smem_groups_max = force_stream ? 0 : std::max<int64_t>(0, (smem_optin - fixed) / group_bytes);
     int n_smem = (int)std::min<int64_t>(ng, smem_groups_max);
     int rem = ng - n_smem;
-    int n_tmem = std::min(rem, tmem_max);
+    int n_tmem = force_stream ? 0 : std::min(rem, tmem_max);
     rem -= n_tmem;
-    int n_rf = std::min(rem, rf_max);
+    int n_rf = force_stream ? 0 : std::min(rem, rf_max);
     rem -= n_rf;
     if (rem > 0 && !allow_stream) return false;
     const int n_stream = rem;
@@ -157,6 +158,11 @@ Plan make_plan(int64_t V, int r, int kind, int Bcap, int NH, int sm_count, int s
   };
 
   int G;
+  if (force_stream) {
+    G = grid_req > 0 ? std::min(grid_req, sm_count) : sm_count;
+    if (!fits(G, P, true)) P.ok = false;
+    return P;
+  }
   if (grid_req > 0) {
     G = std::min(grid_req, sm_count);
     if (!fits(G, P, true)) P.ok = false;
@@ -298,10 +304,11 @@ int whead_create(const void* W, const void* E, const whead_params* params, whead
   h->slots_per_parity = 2 * (int64_t)h->sm_count * kMaxB;
 
   // placements: walks <= 8 (one n8 half) and, if asked for, walks <= 16
-  h->plan[0] = make_plan(p.V, p.r, p.kind, std::min(p.max_B, 8), 1, h->sm_count, h->smem_optin, p.grid);
+  const bool force_stream = (p.flags & WHEAD_FLAG_FORCE_STREAM) != 0u;
+  h->plan[0] = make_plan(p.V, p.r, p.kind, std::min(p.max_B, 8), 1, h->sm_count, h->smem_optin, p.grid, force_stream);
   if (!h->plan[0].ok) return fail(WHEAD_ERR_UNSUPPORTED);
   if (p.max_B > 8) {
-    h->plan[1] = make_plan(p.V, p.r, p.kind, p.max_B, 2, h->sm_count, h->smem_optin, p.grid);
+    h->plan[1] = make_plan(p.V, p.r, p.kind, p.max_B, 2, h->sm_count, h->smem_optin, p.grid, force_stream);
     if (!h->plan[1].ok) return fail(WHEAD_ERR_UNSUPPORTED);
   }
 

@@ -16,6 +16,7 @@ RECURRENT = 1
 
 FLAG_LOGITS_F32 = 1 << 0
 FLAG_FIXED_LATENT = 1 << 1
+FLAG_FORCE_STREAM = 1 << 2
 FLAG_FAULT_SKIP_ARRIVAL = 1 << 8
 
 OK = 0

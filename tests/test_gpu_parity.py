@@ -252,3 +252,15 @@ def test_sweep_point_sixteen_walks(torch_cuda):
     print(head.plan(16))
     check_walk(head, d, dd, T=1.0, seed=11)
     head.close()
+
+
+def test_force_stream_parity(torch_cuda):
+    """The fused but non-resident walk (every row of W re-read each step) gives the same walk."""
+    from speculative_decoding_serial_gb300 import whead as wh
+    d = I.make_inputs(O.MARKOV, 50000, 256, 2, 4, seed=31)
+    dd = to_device(d, "cuda")
+    head = make_head(torch_cuda, d, dd, max_B=2, max_gamma=4, flags=wh.FLAG_FORCE_STREAM)
+    plan = head.plan(2)
+    assert plan["smem_groups"] == plan["tmem_groups"] == plan["rf_groups"] == 0 and plan["stream_groups"] > 0
+    check_walk(head, d, dd, T=1.0, seed=3)
+    head.close()
