@@ -288,6 +288,16 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
+// Warp-wide maximum of a 64-bit value split as (hi, lo): redux.sync on the high words, then on the low words
+// of the lanes that hold the maximal high word. Every lane returns the result.
+__device__ __forceinline__ unsigned long long warp_max64(uint32_t hi, uint32_t lo) {
+  uint32_t mh, ml;
+  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(mh) : "r"(hi));
+  const uint32_t l2 = (hi == mh) ? lo : 0u;
+  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(ml) : "r"(l2));
+  return ((unsigned long long)mh << 32) | ml;
+}
+
 __device__ __forceinline__ unsigned long long umax64(unsigned long long a, unsigned long long b) { return a > b ? a : b; }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -771,15 +781,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (sampled) key = __fadd_rn(__fdiv_rn(z, T), gumbel_noise(P.seed, 0u, tau, v));
           bestk = umax64(bestk, pack_key(key, v));
         }
-        uint32_t hi = (uint32_t)(bestk >> 32), lo = (uint32_t)bestk;
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) {
-          const uint32_t ohi = __shfl_xor_sync(0xffffffffu, hi, off), olo = __shfl_xor_sync(0xffffffffu, lo, off);
-          const bool take = (ohi > hi) || (ohi == hi && olo > lo);
-          hi = take ? ohi : hi;
-          lo = take ? olo : lo;
-        }
-        if (lane == 0) s_red[warp * kMaxB] = ((unsigned long long)hi << 32) | lo;
+        const unsigned long long wk = warp_max64((uint32_t)(bestk >> 32), (uint32_t)bestk);
+        if (lane == 0) s_red[warp * kMaxB] = wk;
       } else {
         const int Bp = B == 1 ? 1 : B == 2 ? 2 : B <= 4 ? 4 : B <= 8 ? 8 : 16;
         const int n = tid & (Bp - 1);
@@ -840,56 +843,52 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         const uint64_t t_start = globaltimer_ns();
-        if (lane == 0) {
-          if (!skip) asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(P.cnt) : "memory");
-          const unsigned int target = (unsigned int)(t + 1) * (unsigned int)G;
+        if (lane == 0 && !skip) asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(P.cnt) : "memory");
+        // The counter only says when to look: once all but a few CTAs have arrived, every poll also reads the
+        // slots, and the step is complete exactly when every slot carries this step's tag.
+        constexpr int kSlotsPerLane = kMaxGrid / 32;
+        const unsigned int target = (unsigned int)(t + 1) * (unsigned int)G;
+        const unsigned int near = target - (unsigned int)min(G, 4);
+        bool late = false;
+        for (int n = 0; n < B && !late; ++n) {
+          unsigned long long w[kSlotsPerLane];
+#pragma unroll
+          for (int i = 0; i < kSlotsPerLane; ++i) w[i] = (lane + 32 * i < G) ? 0ull : tag;  // tag 0: not read yet
           uint32_t spins = 0;
+          bool counted = (n > 0);  // later walks: everyone has arrived already
           while (true) {
-            unsigned int now;
-            asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(now) : "l"(P.cnt) : "memory");
-            if (now >= target) break;
-            if ((++spins & 31u) == 0u && globaltimer_ns() - t_start > P.timeout_ns) {
-              *s_abort = 1;
+            if (!counted) {
+              unsigned int now = 0;
+              if (lane == 0) asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(now) : "l"(P.cnt) : "memory");
+              now = __shfl_sync(0xffffffffu, now, 0);
+              counted = now >= near;
+            }
+            bool fresh = true;
+            if (counted) {
+#pragma unroll
+              for (int i = 0; i < kSlotsPerLane; ++i) {
+                const int cc = lane + 32 * i;
+                if (cc < G && (w[i] >> 56) != (unsigned long long)(t + 1))
+                  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w[i]) : "l"(sl + (int64_t)cc * B + n) : "memory");
+              }
+#pragma unroll
+              for (int i = 0; i < kSlotsPerLane; ++i) fresh = fresh && ((w[i] >> 56) == (unsigned long long)(t + 1));
+            }
+            if (__all_sync(0xffffffffu, counted && fresh)) break;
+            // the time-out decision is made by the whole warp at once, so the lanes leave the loop together
+            if ((++spins & 15u) == 0u && __any_sync(0xffffffffu, globaltimer_ns() - t_start > P.timeout_ns)) {
+              late = true;
               break;
             }
           }
-        }
-        __syncwarp();
-        bool late = *s_abort != 0;
-        for (int n = 0; n < B && !late; ++n) {
-          // all of this lane's slots (CTAs lane, lane + 32, ...) are requested at once; only words that do not
-          // carry this step's tag yet are read again
-          constexpr int kSlotsPerLane = kMaxGrid / 32;
-          unsigned long long w[kSlotsPerLane];
-#pragma unroll
-          for (int i = 0; i < kSlotsPerLane; ++i) {
-            const int cc = lane + 32 * i;
-            w[i] = tag;
-            if (cc < G)
-              asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w[i]) : "l"(sl + (int64_t)cc * B + n) : "memory");
-          }
+          late = __any_sync(0xffffffffu, late);
+          if (late) break;
           unsigned long long best = 0ull;
 #pragma unroll
-          for (int i = 0; i < kSlotsPerLane; ++i) {
-            const int cc = lane + 32 * i;
-            uint32_t spins = 0;
-            while ((w[i] >> 56) != (unsigned long long)(t + 1) && !late) {
-              asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w[i]) : "l"(sl + (int64_t)cc * B + n) : "memory");
-              if ((++spins & 31u) == 0u && globaltimer_ns() - t_start > P.timeout_ns) late = true;
-            }
-            best = umax64(best, w[i] & 0x00FFFFFFFFFFFFFFull);
-          }
-          uint32_t hi = (uint32_t)(best >> 32), lo = (uint32_t)best;
-#pragma unroll
-          for (int off = 16; off >= 1; off >>= 1) {
-            const uint32_t ohi = __shfl_xor_sync(0xffffffffu, hi, off), olo = __shfl_xor_sync(0xffffffffu, lo, off);
-            const bool take = (ohi > hi) || (ohi == hi && olo > lo);
-            hi = take ? ohi : hi;
-            lo = take ? olo : lo;
-          }
-          late = __any_sync(0xffffffffu, late);
-          if (lane == 0 && !late) {
-            const int32_t x = (int32_t)(0xFFFFFFu - (lo & 0xFFFFFFu));
+          for (int i = 0; i < kSlotsPerLane; ++i) best = umax64(best, w[i] & 0x00FFFFFFFFFFFFFFull);
+          const unsigned long long wk = warp_max64((uint32_t)(best >> 32), (uint32_t)best);
+          if (lane == 0) {
+            const int32_t x = (int32_t)(0xFFFFFFu - ((uint32_t)wk & 0xFFFFFFu));
             s_win[n] = x;
             if (cta == 0) P.tokens[(int64_t)n * gamma + t] = x;
           }
