@@ -54,17 +54,18 @@ def recorded_traffic():
 
 
 def probe_onchip():
-    """Shared/tensor-memory bytes per SM clock, mma.sync clocks per op and grid-exchange clocks (measured)."""
+    """Shared/tensor-memory bytes per SM clock, mma.sync and thin-N tcgen05.mma clocks per op, grid-exchange clocks."""
     import ctypes
     from speculative_decoding_serial_gb300 import build
     try:
         L = ctypes.CDLL(build.PROBE_LIB)
-        out = (ctypes.c_double * 4)()
+        out = (ctypes.c_double * 6)()
         rc = L.whead_probe_onchip(out)
         if rc != 0:
             return None
         return {"smem_b_per_clk": out[0], "tmem_b_per_clk": out[1], "mma_m16n8k16_clk_per_sm": out[2],
-                "grid_exchange_clk": out[3]}
+                "grid_exchange_clk": out[3], "tcgen05_m128n16k16_clk_1_issuer": out[4],
+                "tcgen05_m128n16k16_clk_4_issuers": out[5]}
     except OSError:
         return None
 

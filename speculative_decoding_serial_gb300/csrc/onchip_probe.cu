@@ -1,11 +1,16 @@
 // onchip_probe.cu — measures the per-SM figures the walk's on-chip roofline is expressed in.
 //
 // Built as a separate library (libwhead_probe.so) for the benchmark; the walk library does not use it.
-//   whead_probe_onchip(out[4]):
+//   whead_probe_onchip(out[6]):
 //     out[0] shared-memory read bandwidth, bytes per SM clock (ld.shared.v4, 384 threads, 192 KB resident)
 //     out[1] tensor-memory read bandwidth, bytes per SM clock (tcgen05.ld.32x32b.x32, 384 threads, 512 cols)
 //     out[2] SM clocks per mma.sync.m16n8k16 bf16 -> fp32 per SM (independent accumulators, 384 threads)
 //     out[3] SM clocks per grid-wide arrival + wait over all SMs (relaxed counter; cooperative launch)
+//     out[4] SM clocks per tcgen05.mma.cta_group::1.kind::f16 of shape M128 N16 K16 (A and B in shared memory,
+//            128-byte swizzle, D in tensor memory), one issuing thread
+//     out[5] the same with four issuing threads (one per warp, separate accumulators)
+// The last two say how fast the fifth-generation tensor core consumes a thin (N <= 16) operand: W bytes per
+// clock = 4096 / out[5], against 256 B per clock for mma.sync.m16n8k16 at out[2] = 2.
 // Every wait is bounded; every access stays inside its buffer. Returns 0, or a negative CUDA error.
 #include <cuda_runtime.h>
 
@@ -129,6 +134,91 @@ __global__ void __launch_bounds__(kThreads, 1) grid_exchange(unsigned int* count
   if (threadIdx.x == 0) cyc[blockIdx.x] = t1 - t0;
 }
 
+// --- tcgen05.mma issue rate at a thin N ---
+constexpr int kUmmaABytes = 128 * 256 * 2;  // one 128 x 256 bf16 tile, [k/64][128 rows][128 B], 128-byte swizzle
+constexpr int kUmmaBBytes = 16 * 256 * 2;   // 16 x 256 bf16, [k/64][16 rows][128 B]
+constexpr int kUmmaSmem = kUmmaABytes + kUmmaBBytes + 1024 + 64;
+
+__device__ __forceinline__ uint64_t umma_sdesc(uint32_t addr) {
+  return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)1u << 16) | ((uint64_t)(1024u >> 4) << 32) |
+         ((uint64_t)1u << 46) | ((uint64_t)2u << 61);
+}
+
+// NW threads (lane 0 of warps 0..NW-1) each issue 2 tiles x 16 K-steps of M128 N16 K16 into their own columns,
+// commit to their own mbarrier and wait (bounded by 100 ms of global time). cyc[block] = issuer 0's median.
+template <int NW>
+__global__ void __launch_bounds__(128, 1) umma_rate(long long* cyc, int* status, int reps) {
+  extern __shared__ uint8_t umma_smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(umma_smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + kUmmaABytes + kUmmaBBytes);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(mbar + 4);
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  for (int i = tid; i < (kUmmaABytes + kUmmaBBytes) / 16; i += blockDim.x) reinterpret_cast<uint4*>(sm)[i] = make_uint4(0, 0, 0, 0);
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"((uint32_t)__cvta_generic_to_shared(s_tmem)),
+                 "r"(256) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (tid < 4) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"((uint32_t)__cvta_generic_to_shared(mbar + tid)) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *s_tmem;
+  __shared__ long long s_med[16];
+  if (warp < NW && lane == 0) {
+    // instruction descriptor: D f32, A and B bf16, both K-major, N = 16, M = 128
+    const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
+    const uint32_t a0 = (uint32_t)__cvta_generic_to_shared(sm), b0 = a0 + kUmmaABytes;
+    const uint32_t mb = (uint32_t)__cvta_generic_to_shared(mbar + warp);
+    for (int rep = 0; rep < reps && rep < 16; ++rep) {
+      const long long t0 = clock64();
+#pragma unroll 1
+      for (int d = 0; d < 2; ++d) {
+        const uint32_t dcol = tmem + (uint32_t)((warp * 2 + d) * 16);
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+          const uint64_t ad = umma_sdesc(a0 + (uint32_t)((kk / 4) * 128 * 128 + (kk % 4) * 32));
+          const uint64_t bd = umma_sdesc(b0 + (uint32_t)((kk / 4) * 16 * 128 + (kk % 4) * 32));
+          asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+                       ::"r"(dcol), "l"(ad), "l"(bd), "r"(idesc), "r"(kk > 0 ? 1u : 0u) : "memory");
+        }
+      }
+      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mb) : "memory");
+      bool ok = false;
+      uint64_t ts, tn;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(ts));
+      tn = ts;
+      while (!ok && tn - ts < 100000000ull) {
+        uint32_t r;
+        asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+                     : "=r"(r) : "r"(mb), "r"((uint32_t)(rep & 1)) : "memory");
+        ok = r != 0;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(tn));
+      }
+      if (warp == 0) s_med[rep] = clock64() - t0;
+      if (!ok) {
+        atomicExch(status, 1);
+        break;
+      }
+    }
+  }
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (tid == 0) {
+    // median of repetitions 2.. (the first two warm up)
+    long long v[16];
+    const int n = (reps < 16 ? reps : 16) - 2;
+    for (int i = 0; i < n; ++i) v[i] = s_med[i + 2];
+    for (int i = 1; i < n; ++i)
+      for (int j = i; j > 0 && v[j - 1] > v[j]; --j) { const long long x = v[j]; v[j] = v[j - 1]; v[j - 1] = x; }
+    cyc[blockIdx.x] = v[n / 2];
+  }
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256) : "memory");
+}
+
 double median_cycles(const long long* d_cyc, int n) {
   std::vector<long long> h(n);
   if (cudaMemcpy(h.data(), d_cyc, n * sizeof(long long), cudaMemcpyDeviceToHost) != cudaSuccess) return -1.0;
@@ -179,6 +269,20 @@ extern "C" int whead_probe_onchip(double* out) {
     int st = 0;
     cudaMemcpy(&st, d_status, 4, cudaMemcpyDeviceToHost);
     out[3] = st ? -1.0 : median_cycles(d_cyc, nsm) / iters;
+    // 120 KB of dynamic shared memory keeps one CTA per SM (the kernel uses the first 74 KB)
+    const int umma_smem = 120 * 1024;
+    static_assert(kUmmaSmem <= 120 * 1024, "umma probe layout");
+    if (cudaFuncSetAttribute(umma_rate<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, umma_smem) != cudaSuccess ||
+        cudaFuncSetAttribute(umma_rate<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, umma_smem) != cudaSuccess) { rc = -3; break; }
+    if (cudaMemset(d_status, 0, 4) != cudaSuccess) { rc = -4; break; }
+    umma_rate<1><<<nsm, 128, umma_smem>>>(d_cyc, d_status, 12);
+    if (cudaDeviceSynchronize() != cudaSuccess) { rc = -4; break; }
+    out[4] = median_cycles(d_cyc, nsm) / 32.0;
+    umma_rate<4><<<nsm, 128, umma_smem>>>(d_cyc, d_status, 12);
+    if (cudaDeviceSynchronize() != cudaSuccess) { rc = -4; break; }
+    out[5] = median_cycles(d_cyc, nsm) / 128.0;
+    cudaMemcpy(&st, d_status, 4, cudaMemcpyDeviceToHost);
+    if (st) out[4] = out[5] = -1.0;
   } while (false);
   if (d_out) cudaFree(d_out);
   if (d_cyc) cudaFree(d_cyc);
