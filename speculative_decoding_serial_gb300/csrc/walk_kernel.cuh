@@ -656,10 +656,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
 
+      // the next group's work-list entry and this group's base logits are read a group ahead / at the start, so
+      // neither latency sits between a group's last mma and its epilogue
+      uint32_t ent_next = __shfl_sync(0xffffffffu, my_entry, 0);
       for (int e = 0; e < my_count; ++e) {
-        const uint32_t ent = __shfl_sync(0xffffffffu, my_entry, e);
+        const uint32_t ent = ent_next;
+        ent_next = __shfl_sync(0xffffffffu, my_entry, (e + 1) & 31);
         const int j = (int)(ent & 0xFFu);
         const uint32_t tier = (ent >> 8) & 3u;
+        float zb0 = 0.f, zb1 = 0.f;
+        if constexpr (NB1) {
+          zb0 = s_base[kGroupRows * j + g];
+          zb1 = s_base[kGroupRows * j + g + 8];
+        }
 
         float acc[4][NH][4];
         if (tier == kTierSmem) {
@@ -743,10 +752,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (NB1) {
           if (c == 0) {
             s_base[lr0] = __fadd_rn(__fadd_rn(__fadd_rn(acc[0][0][0], acc[1][0][0]), __fadd_rn(acc[2][0][0], acc[3][0][0])),
-                                    s_base[lr0]);
+                                    zb0);
             s_base[lr0 + 8] =
-                __fadd_rn(__fadd_rn(__fadd_rn(acc[0][0][2], acc[1][0][2]), __fadd_rn(acc[2][0][2], acc[3][0][2])),
-                          s_base[lr0 + 8]);
+                __fadd_rn(__fadd_rn(__fadd_rn(acc[0][0][2], acc[1][0][2]), __fadd_rn(acc[2][0][2], acc[3][0][2])), zb1);
           }
         } else {
 #pragma unroll
