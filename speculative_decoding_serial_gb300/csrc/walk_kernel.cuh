@@ -778,16 +778,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int valid = (int)min((int64_t)rows_cta, V - row_base);
         const int64_t obase = (int64_t)t * V + row_base;
         unsigned long long bestk = 0ull;
-        for (int lr = tid; lr < valid; lr += kThreads) {
-          const float z = s_base[lr];
-          if (P.logits) {
-            if (want_f32) reinterpret_cast<float*>(P.logits)[obase + lr] = z;
-            else reinterpret_cast<__nv_bfloat16*>(P.logits)[obase + lr] = __float2bfloat16_rn(z);
+        if (!sampled && !P.logits) {
+          // greedy without logits: keys only (a loop of its own, so it carries no sampling code)
+#pragma unroll 4
+          for (int lr = tid; lr < valid; lr += kThreads)
+            bestk = umax64(bestk, pack_key(s_base[lr], (uint32_t)(row_base + lr)));
+        } else {
+          for (int lr = tid; lr < valid; lr += kThreads) {
+            const float z = s_base[lr];
+            if (P.logits) {
+              if (want_f32) reinterpret_cast<float*>(P.logits)[obase + lr] = z;
+              else reinterpret_cast<__nv_bfloat16*>(P.logits)[obase + lr] = __float2bfloat16_rn(z);
+            }
+            const uint32_t v = (uint32_t)(row_base + lr);
+            float key = z;
+            if (sampled) key = __fadd_rn(__fdiv_rn(z, T), gumbel_noise(P.seed, 0u, tau, v));
+            bestk = umax64(bestk, pack_key(key, v));
           }
-          const uint32_t v = (uint32_t)(row_base + lr);
-          float key = z;
-          if (sampled) key = __fadd_rn(__fdiv_rn(z, T), gumbel_noise(P.seed, 0u, tau, v));
-          bestk = umax64(bestk, pack_key(key, v));
         }
         const unsigned long long wk = warp_max64((uint32_t)(bestk >> 32), (uint32_t)bestk);
         if (lane == 0) s_red[warp * kMaxB] = wk;
@@ -800,16 +807,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float* zrow = s_base + n * rows_cta;
           const int valid = (int)min((int64_t)rows_cta, V - row_base);
           const int64_t obase = ((int64_t)n * gamma + t) * V + row_base;
-          for (int lr = tid / Bp; lr < valid; lr += stride) {
-            const float z = zrow[lr];
-            if (P.logits) {
-              if (want_f32) reinterpret_cast<float*>(P.logits)[obase + lr] = z;
-              else reinterpret_cast<__nv_bfloat16*>(P.logits)[obase + lr] = __float2bfloat16_rn(z);
+          if (!sampled && !P.logits) {
+#pragma unroll 4
+            for (int lr = tid / Bp; lr < valid; lr += stride)
+              bestk = umax64(bestk, pack_key(zrow[lr], (uint32_t)(row_base + lr)));
+          } else {
+            for (int lr = tid / Bp; lr < valid; lr += stride) {
+              const float z = zrow[lr];
+              if (P.logits) {
+                if (want_f32) reinterpret_cast<float*>(P.logits)[obase + lr] = z;
+                else reinterpret_cast<__nv_bfloat16*>(P.logits)[obase + lr] = __float2bfloat16_rn(z);
+              }
+              const uint32_t v = (uint32_t)(row_base + lr);
+              float key = z;
+              if (sampled) key = __fadd_rn(__fdiv_rn(z, T), gumbel_noise(P.seed, (uint32_t)n, tau, v));
+              bestk = umax64(bestk, pack_key(key, v));
             }
-            const uint32_t v = (uint32_t)(row_base + lr);
-            float key = z;
-            if (sampled) key = __fadd_rn(__fdiv_rn(z, T), gumbel_noise(P.seed, (uint32_t)n, tau, v));
-            bestk = umax64(bestk, pack_key(key, v));
           }
         }
         for (int off = 16; off >= Bp; off >>= 1) bestk = umax64(bestk, __shfl_xor_sync(0xffffffffu, bestk, off));
