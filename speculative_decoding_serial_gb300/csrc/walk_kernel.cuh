@@ -846,11 +846,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         unsigned long long kk = 0ull;
         if (lane < B)
           for (int w = 0; w < kWarps; ++w) kk = umax64(kk, s_red[w * kMaxB + lane]);
-        // the E row of this CTA's candidate goes to L2 now: if it wins, every CTA reads it right after the wait
-        if (lane < B && kk != 0ull && !(P.flags & kFlagFixedLatent)) {
-          const uint16_t* er = P.E + (int64_t)(0xFFFFFFFFu - (uint32_t)(kk & 0xFFFFFFFFull)) * r;
-          for (int off = 0; off < r * 2; off += 128) prefetch_l2(reinterpret_cast<const uint8_t*>(er) + off);
-        }
         unsigned long long* sl = P.slots + (int64_t)(t & 1) * G * B;
         const unsigned long long tag = (unsigned long long)(t + 1) << 56;
         const bool skip = (P.flags & kFlagSkipArrival) && cta == 0 && t == 0;
@@ -865,6 +860,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         const uint64_t t_start = globaltimer_ns();
         if (lane == 0 && !skip) asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(P.cnt) : "memory");
+        // the E row of this CTA's candidate goes to L2 while the others arrive: if it wins, every CTA reads it
+        // right after the wait (issued after the arrival so that it cannot hold the arrival back)
+        if (lane < B && kk != 0ull && !(P.flags & kFlagFixedLatent)) {
+          const uint16_t* er = P.E + (int64_t)(0xFFFFFFFFu - (uint32_t)(kk & 0xFFFFFFFFull)) * r;
+          for (int off = 0; off < r * 2; off += 128) prefetch_l2(reinterpret_cast<const uint8_t*>(er) + off);
+        }
         // The counter only says when to look: once all but a few CTAs have arrived, every poll also reads the
         // slots, and the step is complete exactly when every slot carries this step's tag.
         constexpr int kSlotsPerLane = kMaxGrid / 32;
