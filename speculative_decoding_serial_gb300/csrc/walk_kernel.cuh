@@ -844,8 +844,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       // arrived at step t + 1, that is, after every CTA has finished reading step t's buffer.
       if (!RFW && warp == 0) {
         unsigned long long kk = 0ull;
-        if (lane < B)
-          for (int w = 0; w < kWarps; ++w) kk = umax64(kk, s_red[w * kMaxB + lane]);
+        if constexpr (NB1) {
+          // one walk: lane w reads warp w's key, and the warp maximum goes to every lane
+          const unsigned long long mine = (lane < kWarps) ? s_red[lane * kMaxB] : 0ull;
+          kk = warp_max64((uint32_t)(mine >> 32), (uint32_t)mine);
+        } else {
+          if (lane < B)
+            for (int w = 0; w < kWarps; ++w) kk = umax64(kk, s_red[w * kMaxB + lane]);
+        }
         unsigned long long* sl = P.slots + (int64_t)(t & 1) * G * B;
         const unsigned long long tag = (unsigned long long)(t + 1) << 56;
         const bool skip = (P.flags & kFlagSkipArrival) && cta == 0 && t == 0;
