@@ -248,12 +248,16 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 ctr, uint32_t k0, uint32_t 
 
 // Standard Gumbel noise for (seed, walk b, absolute step tau, row v): counter (v/4, tau, b, 0), word v%4,
 // U = ((w >> 9) + 0.5) * 2^-23 (exact in fp32), g = -log(-log U).
-__device__ __forceinline__ float gumbel_noise(uint64_t seed, uint32_t b, uint32_t tau, uint32_t v) {
-  const uint4 o = philox4x32_10(make_uint4(v >> 2, tau, b, 0u), (uint32_t)seed, (uint32_t)(seed >> 32));
-  const uint32_t sel = v & 3u;
-  const uint32_t w = sel == 0 ? o.x : sel == 1 ? o.y : sel == 2 ? o.z : o.w;
+// Gumbel noise from one Philox output word: U = ((w >> 9) + 1/2) 2^-23 lies strictly inside (0, 1).
+__device__ __forceinline__ float gumbel_from_word(uint32_t w) {
   const float u = __fmul_rn(__fadd_rn(__uint2float_rn(w >> 9), 0.5f), 0x1p-23f);
   return -logf(-logf(u));
+}
+
+// The four rows 4q .. 4q + 3 of walk b at step tau share one Philox call (counter (q, tau, b, 0)): row v
+// takes output word v % 4.
+__device__ __forceinline__ uint4 philox_quad(uint64_t seed, uint32_t b, uint32_t tau, uint32_t q) {
+  return philox4x32_10(make_uint4(q, tau, b, 0u), (uint32_t)seed, (uint32_t)(seed >> 32));
 }
 
 // Order-preserving map of an fp32 key to uint32 (negative: bitwise not; else set the sign bit; -0 -> +0),
@@ -783,17 +787,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 4
           for (int lr = tid; lr < valid; lr += kThreads)
             bestk = umax64(bestk, pack_key(s_base[lr], (uint32_t)(row_base + lr)));
-        } else {
+        } else if (!sampled) {
           for (int lr = tid; lr < valid; lr += kThreads) {
             const float z = s_base[lr];
-            if (P.logits) {
-              if (want_f32) reinterpret_cast<float*>(P.logits)[obase + lr] = z;
-              else reinterpret_cast<__nv_bfloat16*>(P.logits)[obase + lr] = __float2bfloat16_rn(z);
+            if (want_f32) reinterpret_cast<float*>(P.logits)[obase + lr] = z;
+            else reinterpret_cast<__nv_bfloat16*>(P.logits)[obase + lr] = __float2bfloat16_rn(z);
+            bestk = umax64(bestk, pack_key(z, (uint32_t)(row_base + lr)));
+          }
+        } else {
+          // sampled: each thread scores four consecutive rows with one Philox call (the CTA's first row is a
+          // multiple of 16, so row_base + lr is a multiple of 4)
+          for (int lr = 4 * tid; lr < valid; lr += 4 * kThreads) {
+            const float4 z4 = *reinterpret_cast<const float4*>(s_base + lr);
+            const float zz[4] = {z4.x, z4.y, z4.z, z4.w};
+            const uint32_t v0 = (uint32_t)(row_base + lr);
+            const uint4 o = philox_quad(P.seed, 0u, tau, v0 >> 2);
+            const uint32_t ww[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              if (lr + u < valid) {
+                if (P.logits) {
+                  if (want_f32) reinterpret_cast<float*>(P.logits)[obase + lr + u] = zz[u];
+                  else reinterpret_cast<__nv_bfloat16*>(P.logits)[obase + lr + u] = __float2bfloat16_rn(zz[u]);
+                }
+                const float key = __fadd_rn(__fdiv_rn(zz[u], T), gumbel_from_word(ww[u]));
+                bestk = umax64(bestk, pack_key(key, v0 + (uint32_t)u));
+              }
             }
-            const uint32_t v = (uint32_t)(row_base + lr);
-            float key = z;
-            if (sampled) key = __fadd_rn(__fdiv_rn(z, T), gumbel_noise(P.seed, 0u, tau, v));
-            bestk = umax64(bestk, pack_key(key, v));
           }
         }
         const unsigned long long wk = warp_max64((uint32_t)(bestk >> 32), (uint32_t)bestk);
@@ -811,17 +831,32 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll 4
             for (int lr = tid / Bp; lr < valid; lr += stride)
               bestk = umax64(bestk, pack_key(zrow[lr], (uint32_t)(row_base + lr)));
-          } else {
+          } else if (!sampled) {
             for (int lr = tid / Bp; lr < valid; lr += stride) {
               const float z = zrow[lr];
-              if (P.logits) {
-                if (want_f32) reinterpret_cast<float*>(P.logits)[obase + lr] = z;
-                else reinterpret_cast<__nv_bfloat16*>(P.logits)[obase + lr] = __float2bfloat16_rn(z);
+              if (want_f32) reinterpret_cast<float*>(P.logits)[obase + lr] = z;
+              else reinterpret_cast<__nv_bfloat16*>(P.logits)[obase + lr] = __float2bfloat16_rn(z);
+              bestk = umax64(bestk, pack_key(z, (uint32_t)(row_base + lr)));
+            }
+          } else {
+            // sampled: four consecutive rows per Philox call, as for a single walk
+            for (int lr = 4 * (tid / Bp); lr < valid; lr += 4 * stride) {
+              const float4 z4 = *reinterpret_cast<const float4*>(zrow + lr);
+              const float zz[4] = {z4.x, z4.y, z4.z, z4.w};
+              const uint32_t v0 = (uint32_t)(row_base + lr);
+              const uint4 o = philox_quad(P.seed, (uint32_t)n, tau, v0 >> 2);
+              const uint32_t ww[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                if (lr + u < valid) {
+                  if (P.logits) {
+                    if (want_f32) reinterpret_cast<float*>(P.logits)[obase + lr + u] = zz[u];
+                    else reinterpret_cast<__nv_bfloat16*>(P.logits)[obase + lr + u] = __float2bfloat16_rn(zz[u]);
+                  }
+                  const float key = __fadd_rn(__fdiv_rn(zz[u], T), gumbel_from_word(ww[u]));
+                  bestk = umax64(bestk, pack_key(key, v0 + (uint32_t)u));
+                }
               }
-              const uint32_t v = (uint32_t)(row_base + lr);
-              float key = z;
-              if (sampled) key = __fadd_rn(__fdiv_rn(z, T), gumbel_noise(P.seed, (uint32_t)n, tau, v));
-              bestk = umax64(bestk, pack_key(key, v));
             }
           }
         }
