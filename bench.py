@@ -536,6 +536,62 @@ def ablation(args):
                           "us_per_step_slope": sl, "entry_intercept_us": ic, "placement": plan}), flush=True)
 
 
+def placement(args):
+    """Placement sweep on GB300 (Fig. 12 of the pages): per-step cost and entry for chosen splits of a CTA's
+    16-row groups over shared memory, tensor memory and registers, the rest streamed from L2/HBM every step
+    (WHEAD_FLAG_PLACEMENT_CAPS). Complete-call latency over gamma in {1, 7, 16}, least-squares slope and
+    intercept, as for the ablation. One JSON line per split."""
+    import numpy as np
+    import torch
+
+    import whead_inputs as I
+    from speculative_decoding_serial_gb300 import build
+    from speculative_decoding_serial_gb300 import whead as wh
+
+    build.build()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    w = I.WORKLOADS[args.workload]
+    d = I.workload_inputs(args.workload)
+    B, G16 = w["B"], w["gamma"]
+    W = torch.from_numpy(d["W"].view(np.int16)).view(torch.bfloat16).to(dev)
+    E = torch.from_numpy(d["E"].view(np.int16)).view(torch.bfloat16).to(dev)
+    base = torch.from_numpy(d["base"]).to(dev)
+    s0 = torch.from_numpy(d["s0"]).to(dev)
+    A = None if d["A"] is None else torch.from_numpy(d["A"]).to(dev)
+    c = None if d["c"] is None else torch.from_numpy(d["c"]).to(dev)
+    gammas = [g for g in (1, 7, 16) if g <= G16]
+    # (shared, tensor, register) caps; None = the planner's own (fully resident) split
+    splits = [None, (64, 64, 0), (64, 16, 8), (64, 0, 8), (13, 64, 8), (0, 64, 8), (0, 0, 8), (0, 0, 0)]
+    for caps in splits:
+        head = wh.Head(W, E, kind=w["kind"], A=A, c=c, max_B=B, max_gamma=G16, stream=stream, caps=caps)
+        plan = head.plan(B)
+        ys = []
+        for g in gammas:
+            bg = base[:, :g].contiguous()
+            tok = torch.empty((B, g), dtype=torch.int32, device=dev)
+            for _ in range(3):
+                head.walk(bg, s0, T=w["T"], out_tokens=tok)
+            ts = []
+            for _ in range(args.sweep_walks):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                head.walk(bg, s0, T=w["T"], out_tokens=tok)
+                e1.record(stream)
+                e1.synchronize()
+                ts.append(e0.elapsed_time(e1) * 1e3)
+            ys.append(statistics.median(ts))
+        status = head.status()
+        head.close()
+        xm, ym = sum(gammas) / len(gammas), sum(ys) / len(ys)
+        sl = sum((a - xm) * (b - ym) for a, b in zip(gammas, ys)) / sum((a - xm) ** 2 for a in gammas)
+        print(json.dumps({"placement_caps": caps, "workload": args.workload, "status": status, "gammas": gammas,
+                          "us_per_walk": ys, "us_per_step_slope": sl, "entry_intercept_us": ym - sl * xm,
+                          "placement": plan}), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -548,7 +604,11 @@ def main():
     ap.add_argument("--sweep", action="store_true", help="latency of every workload of the pages (one line each)")
     ap.add_argument("--sweep-walks", type=int, default=100)
     ap.add_argument("--ablation", action="store_true", help="fusion vs residency (resident / fused streaming / step-wise)")
+    ap.add_argument("--placement", action="store_true", help="placement sweep over shared/tensor/register tiers")
     args = ap.parse_args()
+    if args.placement:
+        placement(args)
+        return
     if args.sweep:
         sweep(args)
         return

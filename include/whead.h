@@ -51,6 +51,11 @@ typedef enum { WHEAD_MARKOV = 0, WHEAD_RECURRENT = 1 } whead_kind;
 #define WHEAD_FLAG_FIXED_LATENT (1u << 1)    /* measurement mode: never advance the state (Fig. 13b probe) */
 #define WHEAD_FLAG_FORCE_STREAM (1u << 2)    /* measurement mode: keep no row of W on chip; every step re-reads all
                                                 of W from L2/HBM (the fused but non-resident walk of Figs. 4, 11) */
+#define WHEAD_FLAG_PLACEMENT_CAPS (1u << 3)  /* measurement mode (Fig. 12's placement sweep): cap_smem, cap_tmem and
+                                                cap_rf bound the 16-row groups per CTA that shared memory, tensor
+                                                memory and registers may hold; the rest are streamed. Without the
+                                                flag the planner fills shared memory, then tensor memory, then
+                                                registers, and the cap fields are ignored. */
 #define WHEAD_FLAG_FAULT_SKIP_ARRIVAL (1u << 8) /* testing: CTA 0 never arrives at step 0's exchange, so
                                                    every other CTA's bounded wait runs out */
 
@@ -66,6 +71,9 @@ typedef struct {
   uint32_t flags;      /* WHEAD_FLAG_* */
   int32_t grid;        /* number of CTAs; 0 = chosen by the planner (at most one per SM) */
   uint32_t timeout_us; /* limit on every device-side wait; 0 = 1,000,000 us */
+  int32_t cap_smem;    /* with WHEAD_FLAG_PLACEMENT_CAPS: most groups per CTA in shared memory (>= 0) */
+  int32_t cap_tmem;    /* with WHEAD_FLAG_PLACEMENT_CAPS: most groups per CTA in tensor memory (>= 0) */
+  int32_t cap_rf;      /* with WHEAD_FLAG_PLACEMENT_CAPS: most groups per CTA in registers (>= 0) */
 } whead_params;
 
 /* Placement chosen for a batch size (whead_plan_info). Groups are 16 consecutive rows of W. */

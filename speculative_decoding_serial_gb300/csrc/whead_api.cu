@@ -9,6 +9,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <climits>
 #include <cstdio>
 #include <cstring>
 #include <new>
@@ -65,8 +66,10 @@ int kb_of(int r) { return r / 64; }
 
 // Planner: number of CTAs, groups per CTA and their tier; per-warp work lists balanced over the four
 // SM sub-partitions (warp % 4), which each own one tensor core and one quarter of tensor memory.
+// cap_*: most groups per CTA a tier may take (INT_MAX: as many as fit). fixed_tiers: the caps come from the
+// caller (a measurement mode), so the grid is all SMs (or grid_req) and the groups past the caps are streamed.
 Plan make_plan(int64_t V, int r, int kind, int Bcap, int NH, int sm_count, int smem_optin, int grid_req,
-               bool force_stream = false) {
+               int cap_smem = INT_MAX, int cap_tmem = INT_MAX, int cap_rf = INT_MAX, bool fixed_tiers = false) {
   Plan P;
   sm_count = std::min(sm_count, kMaxGrid);
   const int KB = kb_of(r);
@@ -83,12 +86,12 @@ Plan make_plan(int64_t V, int r, int kind, int Bcap, int NH, int sm_count, int s
     const int ra = recurrent ? (r + G - 1) / G : 0;
     const SmemLayout L0 = SmemLayout::make(0, Bcap, r, ra, recurrent, ng);
     const int64_t fixed = 1024 + L0.total;
-    const int64_t smem_groups_max = force_stream ? 0 : std::max<int64_t>(0, (smem_optin - fixed) / group_bytes);
+    const int64_t smem_groups_max = std::min<int64_t>(cap_smem, std::max<int64_t>(0, (smem_optin - fixed) / group_bytes));
     int n_smem = (int)std::min<int64_t>(ng, smem_groups_max);
     int rem = ng - n_smem;
-    int n_tmem = force_stream ? 0 : std::min(rem, tmem_max);
+    int n_tmem = std::min(rem, std::min(tmem_max, cap_tmem));
     rem -= n_tmem;
-    int n_rf = force_stream ? 0 : std::min(rem, rf_max);
+    int n_rf = std::min(rem, std::min(rf_max, cap_rf));
     rem -= n_rf;
     if (rem > 0 && !allow_stream) return false;
     const int n_stream = rem;
@@ -158,7 +161,7 @@ Plan make_plan(int64_t V, int r, int kind, int Bcap, int NH, int sm_count, int s
   };
 
   int G;
-  if (force_stream) {
+  if (fixed_tiers) {
     G = grid_req > 0 ? std::min(grid_req, sm_count) : sm_count;
     if (!fits(G, P, true)) P.ok = false;
     return P;
@@ -304,11 +307,25 @@ int whead_create(const void* W, const void* E, const whead_params* params, whead
   h->slots_per_parity = 2 * (int64_t)h->sm_count * kMaxB;
 
   // placements: walks <= 8 (one n8 half) and, if asked for, walks <= 16
+  // measurement modes: nothing on chip (FORCE_STREAM), or caller-chosen caps per tier (PLACEMENT_CAPS)
+  int cap_s = INT_MAX, cap_t = INT_MAX, cap_r = INT_MAX;
   const bool force_stream = (p.flags & WHEAD_FLAG_FORCE_STREAM) != 0u;
-  h->plan[0] = make_plan(p.V, p.r, p.kind, std::min(p.max_B, 8), 1, h->sm_count, h->smem_optin, p.grid, force_stream);
+  const bool capped = (p.flags & WHEAD_FLAG_PLACEMENT_CAPS) != 0u;
+  if (force_stream) {
+    cap_s = cap_t = cap_r = 0;
+  } else if (capped) {
+    if (p.cap_smem < 0 || p.cap_tmem < 0 || p.cap_rf < 0) return fail(WHEAD_ERR_INVALID_ARG);
+    cap_s = p.cap_smem;
+    cap_t = p.cap_tmem;
+    cap_r = p.cap_rf;
+  }
+  const bool fixed = force_stream || capped;
+  h->plan[0] = make_plan(p.V, p.r, p.kind, std::min(p.max_B, 8), 1, h->sm_count, h->smem_optin, p.grid, cap_s, cap_t,
+                         cap_r, fixed);
   if (!h->plan[0].ok) return fail(WHEAD_ERR_UNSUPPORTED);
   if (p.max_B > 8) {
-    h->plan[1] = make_plan(p.V, p.r, p.kind, p.max_B, 2, h->sm_count, h->smem_optin, p.grid, force_stream);
+    h->plan[1] = make_plan(p.V, p.r, p.kind, p.max_B, 2, h->sm_count, h->smem_optin, p.grid, cap_s, cap_t, cap_r,
+                           fixed);
     if (!h->plan[1].ok) return fail(WHEAD_ERR_UNSUPPORTED);
   }
 

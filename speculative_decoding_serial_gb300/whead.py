@@ -17,6 +17,7 @@ RECURRENT = 1
 FLAG_LOGITS_F32 = 1 << 0
 FLAG_FIXED_LATENT = 1 << 1
 FLAG_FORCE_STREAM = 1 << 2
+FLAG_PLACEMENT_CAPS = 1 << 3
 FLAG_FAULT_SKIP_ARRIVAL = 1 << 8
 
 OK = 0
@@ -37,7 +38,8 @@ class WheadParams(ctypes.Structure):
     _fields_ = [("kind", ctypes.c_int32), ("r", ctypes.c_int32), ("V", ctypes.c_int64),
                 ("A", ctypes.c_void_p), ("c", ctypes.c_void_p), ("max_B", ctypes.c_int32),
                 ("max_gamma", ctypes.c_int32), ("stream", ctypes.c_void_p), ("flags", ctypes.c_uint32),
-                ("grid", ctypes.c_int32), ("timeout_us", ctypes.c_uint32)]
+                ("grid", ctypes.c_int32), ("timeout_us", ctypes.c_uint32), ("cap_smem", ctypes.c_int32),
+                ("cap_tmem", ctypes.c_int32), ("cap_rf", ctypes.c_int32)]
 
 
 class WheadPlan(ctypes.Structure):
@@ -116,18 +118,23 @@ class Head:
     """
 
     def __init__(self, W, E, *, kind=MARKOV, A=None, c=None, max_B=1, max_gamma=16, stream=None, flags=0,
-                 grid=0, timeout_us=0):
+                 grid=0, timeout_us=0, caps=None):
         import torch
         L = load()
         assert W.is_cuda and W.dtype == torch.bfloat16 and W.is_contiguous() and W.dim() == 2
         assert E.shape == W.shape and E.dtype == torch.bfloat16 and E.is_contiguous()
         self.V, self.r = int(W.shape[0]), int(W.shape[1])
+        # caps: (shared, tensor, register) most groups per CTA per tier (placement sweep); the rest stream
+        if caps is not None:
+            flags = int(flags) | FLAG_PLACEMENT_CAPS
+        cs, ct, cr = (int(x) for x in caps) if caps is not None else (0, 0, 0)
         self.kind, self.flags = int(kind), int(flags)
         self._keep = (W, E, A, c)
         self._stream = torch.cuda.current_stream() if stream is None else stream
         p = WheadParams(kind=self.kind, r=self.r, V=self.V, A=_ptr(A), c=_ptr(c), max_B=int(max_B),
                         max_gamma=int(max_gamma), stream=ctypes.c_void_p(self._stream.cuda_stream),
-                        flags=self.flags, grid=int(grid), timeout_us=int(timeout_us))
+                        flags=self.flags, grid=int(grid), timeout_us=int(timeout_us), cap_smem=cs, cap_tmem=ct,
+                        cap_rf=cr)
         h = ctypes.c_void_p()
         _check(L.whead_create(_ptr(W), _ptr(E), ctypes.byref(p), ctypes.byref(h)), "whead_create")
         self._h = h

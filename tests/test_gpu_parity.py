@@ -264,3 +264,39 @@ def test_force_stream_parity(torch_cuda):
     assert plan["smem_groups"] == plan["tmem_groups"] == plan["rf_groups"] == 0 and plan["stream_groups"] > 0
     check_walk(head, d, dd, T=1.0, seed=3)
     head.close()
+
+
+# --- caller-chosen placements (the Fig. 12 placement sweep): any split of a CTA's groups over shared memory,
+# tensor memory and registers, the rest streamed, gives the oracle's walk -------------------------------
+CAPPED = [
+    # B, (shared, tensor, register) caps
+    (1, (4, 4, 2)),
+    (2, (4, 4, 2)),
+    (1, (0, 13, 0)),
+    (3, (0, 0, 3)),
+    (1, (13, 0, 0)),
+    (1, (0, 0, 0)),
+]
+
+
+@pytest.mark.parametrize("B,caps", CAPPED)
+def test_capped_placement_parity(torch_cuda, B, caps):
+    from speculative_decoding_serial_gb300 import whead as wh
+    d = I.make_inputs(O.MARKOV, 30011, 256, B, 4, seed=31 + B)
+    dd = to_device(d, "cuda")
+    head = wh.Head(dd["W"], dd["E"], kind=O.MARKOV, max_B=B, max_gamma=4, flags=wh.FLAG_LOGITS_F32, caps=caps)
+    plan = head.plan(B)
+    assert plan["smem_groups"] <= caps[0] and plan["tmem_groups"] <= caps[1] and plan["rf_groups"] <= caps[2]
+    assert (plan["smem_groups"] + plan["tmem_groups"] + plan["rf_groups"] + plan["stream_groups"]
+            == plan["groups_per_cta"])
+    check_walk(head, d, dd, T=0.0, seed=3)
+    head.close()
+
+
+def test_capped_placement_rejects_negative_caps(torch_cuda):
+    from speculative_decoding_serial_gb300 import whead as wh
+    d = I.make_inputs(O.MARKOV, 1000, 64, 1, 2, seed=1)
+    dd = to_device(d, "cuda")
+    with pytest.raises(wh.WheadError) as e:
+        wh.Head(dd["W"], dd["E"], kind=O.MARKOV, caps=(-1, 0, 0))
+    assert e.value.code == wh.ERR_INVALID_ARG
