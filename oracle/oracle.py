@@ -61,6 +61,21 @@ def lib() -> ctypes.CDLL:
                                             ctypes.c_int32, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
                                             ctypes.c_uint64, vp, vp, vp, vp, vp]
             L.whead_oracle_walk.restype = ctypes.c_int
+            L.whead_oracle_walk_e4m3.argtypes = [ctypes.c_int32, ctypes.c_int64, ctypes.c_int32, vp, vp, vp, vp, vp,
+                                                 vp, vp, ctypes.c_int32, ctypes.c_int32, ctypes.c_int64,
+                                                 ctypes.c_float, ctypes.c_uint64, vp, vp, vp, vp, vp]
+            L.whead_oracle_walk_e4m3.restype = ctypes.c_int
+            L.whead_oracle_e4m3_value.argtypes = [ctypes.c_uint8]
+            L.whead_oracle_e4m3_value.restype = ctypes.c_float
+            L.whead_oracle_e4m3_round.argtypes = [ctypes.c_float]
+            L.whead_oracle_e4m3_round.restype = ctypes.c_uint8
+            L.whead_oracle_quantize_e4m3.argtypes = [vp, ctypes.c_int32, vp]
+            L.whead_oracle_quantize_e4m3.restype = ctypes.c_float
+            L.whead_oracle_split_e4m3.argtypes = [vp, ctypes.c_int32, vp, vp, ctypes.POINTER(ctypes.c_float),
+                                                  ctypes.POINTER(ctypes.c_float)]
+            L.whead_oracle_split_e4m3.restype = None
+            L.whead_oracle_quantize_w_e4m3.argtypes = [vp, ctypes.c_int64, ctypes.c_int32, vp, vp]
+            L.whead_oracle_quantize_w_e4m3.restype = None
             _lib = L
     return _lib
 
@@ -93,12 +108,49 @@ def bf16_round(x: float) -> int:
     return int(lib().whead_oracle_bf16_round(x))
 
 
+def e4m3_value(code: int) -> float:
+    return float(lib().whead_oracle_e4m3_value(int(code) & 0xFF))
+
+
+def e4m3_round(x: float) -> int:
+    return int(lib().whead_oracle_e4m3_round(float(x)))
+
+
+def quantize_e4m3(x):
+    """x: float32 vector. Returns (scale, uint8 E4M3 codes)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    q = np.zeros(x.shape[0], dtype=np.uint8)
+    s = lib().whead_oracle_quantize_e4m3(_ptr(x), x.shape[0], _ptr(q))
+    return float(s), q
+
+
+def split_e4m3(u):
+    """u: float32 vector. Returns (s1, hi codes, s2, lo codes) of the two-vector representation."""
+    u = np.ascontiguousarray(u, dtype=np.float32)
+    hi = np.zeros(u.shape[0], dtype=np.uint8)
+    lo = np.zeros(u.shape[0], dtype=np.uint8)
+    s1, s2 = ctypes.c_float(), ctypes.c_float()
+    lib().whead_oracle_split_e4m3(_ptr(u), u.shape[0], _ptr(hi), _ptr(lo), ctypes.byref(s1), ctypes.byref(s2))
+    return float(s1.value), hi, float(s2.value), lo
+
+
+def quantize_w_e4m3(W):
+    """W: (V, r) uint16 bf16 bits. Returns (Wq (V, r) uint8 E4M3 codes, sw (V,) float32 row scales)."""
+    W = np.ascontiguousarray(W, dtype=np.uint16)
+    V, r = W.shape
+    Wq = np.zeros((V, r), dtype=np.uint8)
+    sw = np.zeros(V, dtype=np.float32)
+    lib().whead_oracle_quantize_w_e4m3(_ptr(W), V, r, _ptr(Wq), _ptr(sw))
+    return Wq, sw
+
+
 def walk(kind, W, E, base, s0, *, A=None, c=None, t0=0, T=0.0, seed=0,
-         want_logits=False, want_z=False, want_gap=True, want_state=False):
+         want_logits=False, want_z=False, want_gap=True, want_state=False, w_e4m3=None):
     """Run the oracle walk.
 
     W, E: (V, r) uint16 bf16 bit patterns. base: (B, gamma, V) float32. s0: (B, r) float32.
-    A: (r, r) float32 and c: (r,) float32 for the recurrent head. Returns a dict with 'tokens'
+    A: (r, r) float32 and c: (r,) float32 for the recurrent head. w_e4m3: None, or (Wq, sw) from
+    quantize_w_e4m3 for the walk with E4M3 weights (W is then only used for its shape). Returns a dict with 'tokens'
     (B, gamma) int32 and, on request, 'logits' (B, gamma, V) uint16 bf16 bits, 'z' float32,
     'gap' (B, gamma) float32 and 'state' (B, gamma, r) float32 (the state after each step).
     """
@@ -124,10 +176,16 @@ def walk(kind, W, E, base, s0, *, A=None, c=None, t0=0, T=0.0, seed=0,
         out["gap"] = np.zeros((B, gamma), dtype=np.float32)
     if want_state:
         out["state"] = np.zeros((B, gamma, r), dtype=np.float32)
-    rc = lib().whead_oracle_walk(int(kind), V, r, _ptr(W), _ptr(E), _ptr(A), _ptr(c), _ptr(base), _ptr(s0),
-                                 B, gamma, int(t0), float(T), int(seed) & 0xFFFFFFFFFFFFFFFF,
-                                 _ptr(out["tokens"]), _ptr(out.get("logits")), _ptr(out.get("z")),
-                                 _ptr(out.get("gap")), _ptr(out.get("state")))
+    tail = (B, gamma, int(t0), float(T), int(seed) & 0xFFFFFFFFFFFFFFFF, _ptr(out["tokens"]),
+            _ptr(out.get("logits")), _ptr(out.get("z")), _ptr(out.get("gap")), _ptr(out.get("state")))
+    if w_e4m3 is None:
+        rc = lib().whead_oracle_walk(int(kind), V, r, _ptr(W), _ptr(E), _ptr(A), _ptr(c), _ptr(base), _ptr(s0), *tail)
+    else:
+        Wq = np.ascontiguousarray(w_e4m3[0], dtype=np.uint8)
+        sw = np.ascontiguousarray(w_e4m3[1], dtype=np.float32)
+        assert Wq.shape == (V, r) and sw.shape == (V,)
+        rc = lib().whead_oracle_walk_e4m3(int(kind), V, r, _ptr(Wq), _ptr(sw), _ptr(E), _ptr(A), _ptr(c), _ptr(base),
+                                          _ptr(s0), *tail)
     if rc != 0:
         raise ValueError(f"oracle walk rejected its arguments (code {rc})")
     return out

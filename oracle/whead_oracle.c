@@ -21,6 +21,12 @@
  *       Markov:    s = E[x]                                   (abstract: Markov heads)
  *       Recurrent: s[i] = tanh(sum_j A[i,j] s[j] + E[x,i] + c[i])  (abstract: recurrent heads)
  *
+ * With E4M3 weights (whead_oracle_walk_e4m3; the pages' Fig. 7 design, int8 on H100, restated with the
+ * 8-bit float format because it is the 8-bit tensor path that is fast on GB300): W is stored as E4M3 codes
+ * with one fp32 scale per row, and each step the state is split into two scaled E4M3 vectors (hi, and the
+ * residual lo) whose projections are scaled and summed:
+ *       p[v]   = sw[v] * (s1 * sum_k Wq[v,k] hi[k] + s2 * sum_k Wq[v,k] lo[k])      fp64, rounded once to fp32
+ *
  * Noise g: Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3",
  * SC'11) with key (seed lo, seed hi) and counter (v/4, tau, b, 0), word v%4; U = ((w>>9)+0.5)*2^-23;
  * g = -logf(-logf(U)).
@@ -97,6 +103,86 @@ float whead_oracle_gumbel(uint64_t seed, int32_t b, int64_t tau, int64_t v) {
 uint16_t whead_oracle_bf16_round(float f) { return bf16_round(f); }
 
 /*
+ * E4M3 (OCP 8-bit floating point, "fn" variant): 1 sign bit, 4 exponent bits with bias 7, 3 mantissa bits,
+ * no infinities, the all-ones code is NaN. Normal values are (1 + m/8) 2^(e-7) for exponent field e = 1..15
+ * (the largest finite value is 1.75 * 2^8 = 448), subnormals are m * 2^-9.
+ */
+float whead_oracle_e4m3_value(uint8_t code) {
+  const int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+  if (e == 15 && m == 7) return NAN;
+  const double mag = (e == 0) ? ldexp((double)m, -9) : ldexp(1.0 + m / 8.0, e - 7);
+  return (float)(sign ? -mag : mag);
+}
+
+/* Nearest E4M3 value to a finite fp32 input, ties to the even mantissa, magnitudes above 448 saturate. */
+uint8_t whead_oracle_e4m3_round(float f) {
+  const uint8_t sign = (uint8_t)((bits_of_f32(f) >> 31) << 7);
+  const double a = fabs((double)f);
+  if (a >= 448.0) return sign | 0x7E;
+  /* the spacing of E4M3 values around a: 2^-9 below 2^-6, else 2^(e-3) in the binade [2^e, 2^(e+1)) */
+  double quantum = ldexp(1.0, -9);
+  if (a >= ldexp(1.0, -6)) {
+    int ex;
+    (void)frexp(a, &ex); /* a = f * 2^ex with f in [0.5, 1) */
+    quantum = ldexp(1.0, (ex - 1) - 3);
+  }
+  const double n = a / quantum; /* exact: quantum is a power of two */
+  double k = floor(n);
+  const double rem = n - k;
+  if (rem > 0.5 || (rem == 0.5 && fmod(k, 2.0) == 1.0)) k += 1.0;
+  const double val = k * quantum;
+  if (val == 0.0) return sign;
+  if (val < ldexp(1.0, -6)) return sign | (uint8_t)(val / ldexp(1.0, -9)); /* subnormal */
+  int ex;
+  const double fr = frexp(val, &ex); /* val = fr * 2^ex, fr in [0.5, 1) */
+  const int e = (ex - 1) + 7;
+  const int m = (int)((fr * 2.0 - 1.0) * 8.0);
+  return sign | (uint8_t)(e << 3) | (uint8_t)m;
+}
+
+/*
+ * Per-vector E4M3 quantization: scale s = max|x| / 448 (fp32), codes q[k] = E4M3(x[k] / s) (fp32 division).
+ * An all-zero vector gets s = 0 and zero codes. Returns s.
+ */
+float whead_oracle_quantize_e4m3(const float* x, int32_t n, uint8_t* q) {
+  float amax = 0.0f;
+  for (int32_t k = 0; k < n; ++k) amax = fabsf(x[k]) > amax ? fabsf(x[k]) : amax;
+  if (amax == 0.0f) {
+    for (int32_t k = 0; k < n; ++k) q[k] = 0;
+    return 0.0f;
+  }
+  const float s = amax / 448.0f;
+  for (int32_t k = 0; k < n; ++k) q[k] = whead_oracle_e4m3_round(x[k] / s);
+  return s;
+}
+
+/*
+ * The state as two E4M3 vectors (Fig. 7 of the pages represents u by two 8-bit vectors whose scaled
+ * products are summed): hi = quantize(u) with scale s1, residual e[k] = u[k] - s1 * value(hi[k]) (fp32
+ * product, then fp32 difference), lo = quantize(e) with scale s2.
+ */
+void whead_oracle_split_e4m3(const float* u, int32_t n, uint8_t* hi, uint8_t* lo, float* s1, float* s2) {
+  float* e = (float*)malloc(sizeof(float) * (size_t)(n > 0 ? n : 1));
+  *s1 = whead_oracle_quantize_e4m3(u, n, hi);
+  for (int32_t k = 0; k < n; ++k) {
+    const float prod = *s1 * whead_oracle_e4m3_value(hi[k]);
+    e[k] = u[k] - prod;
+  }
+  *s2 = whead_oracle_quantize_e4m3(e, n, lo);
+  free(e);
+}
+
+/* W (V x r bf16) to E4M3 codes with one scale per row, each row quantized as a vector. */
+void whead_oracle_quantize_w_e4m3(const uint16_t* W, int64_t V, int32_t r, uint8_t* Wq, float* sw) {
+  float* row = (float*)malloc(sizeof(float) * (size_t)r);
+  for (int64_t v = 0; v < V; ++v) {
+    for (int32_t k = 0; k < r; ++k) row[k] = bf16_value(W[(size_t)v * r + k]);
+    sw[v] = whead_oracle_quantize_e4m3(row, r, Wq + (size_t)v * r);
+  }
+  free(row);
+}
+
+/*
  * One call of the walk.
  *   kind      0 = Markov (s <- E[x]), 1 = recurrent (s <- tanh(A s + E[x] + c))
  *   W, E      V x r bf16 bit patterns, row-major
@@ -109,21 +195,24 @@ uint16_t whead_oracle_bf16_round(float f) { return bf16_round(f); }
  *   gap_out   out or NULL, B x gamma fp32: largest key minus the largest key over the other rows
  *   state_out out or NULL, B x gamma x r fp32: the state after each step's advance
  */
-int whead_oracle_walk(int32_t kind, int64_t V, int32_t r, const uint16_t* W, const uint16_t* E,
-                      const float* A, const float* c, const float* base, const float* s0, int32_t B,
-                      int32_t gamma, int64_t t0, float T, uint64_t seed, int32_t* tokens,
-                      uint16_t* logits, float* z_out, float* gap_out, float* state_out) {
+static int walk_impl(int fp8, int32_t kind, int64_t V, int32_t r, const uint16_t* W, const uint8_t* Wq,
+                     const float* sw, const uint16_t* E, const float* A, const float* c, const float* base,
+                     const float* s0, int32_t B, int32_t gamma, int64_t t0, float T, uint64_t seed,
+                     int32_t* tokens, uint16_t* logits, float* z_out, float* gap_out, float* state_out) {
   if ((kind != 0 && kind != 1) || V < 1 || r < 1 || B < 1 || gamma < 1 || t0 < 0) return ORACLE_EINVAL;
-  if (!W || !E || !base || !s0 || !tokens) return ORACLE_EINVAL;
+  if ((fp8 ? (!Wq || !sw) : !W) || !E || !base || !s0 || !tokens) return ORACLE_EINVAL;
   if (kind == 1 && !A) return ORACLE_EINVAL;
   if (!(T >= 0.0f)) return ORACLE_EINVAL;
 
   float* s = (float*)malloc(sizeof(float) * (size_t)r);
   float* s_next = (float*)malloc(sizeof(float) * (size_t)r);
   double* q = (double*)malloc(sizeof(double) * (size_t)r);
+  double* ql = (double*)malloc(sizeof(double) * (size_t)r);
+  uint8_t* hi = (uint8_t*)malloc((size_t)r);
+  uint8_t* lo = (uint8_t*)malloc((size_t)r);
   float* key = (float*)malloc(sizeof(float) * (size_t)V);
-  if (!s || !s_next || !q || !key) {
-    free(s); free(s_next); free(q); free(key);
+  if (!s || !s_next || !q || !ql || !hi || !lo || !key) {
+    free(s); free(s_next); free(q); free(ql); free(hi); free(lo); free(key);
     return ORACLE_ENOMEM;
   }
 
@@ -134,13 +223,33 @@ int whead_oracle_walk(int32_t kind, int64_t V, int32_t r, const uint16_t* W, con
       const int64_t tau = t0 + t;
       const size_t row_bt = ((size_t)b * (size_t)gamma + (size_t)t) * (size_t)V;
 
-      /* projection input, rounded to bf16 */
-      for (int32_t k = 0; k < r; ++k) q[k] = (double)bf16_value(bf16_round(s[k]));
+      /* projection input: rounded to bf16, or (E4M3 weights) split into two scaled E4M3 vectors */
+      float s1 = 0.0f, s2 = 0.0f;
+      if (!fp8) {
+        for (int32_t k = 0; k < r; ++k) q[k] = (double)bf16_value(bf16_round(s[k]));
+      } else {
+        whead_oracle_split_e4m3(s, r, hi, lo, &s1, &s2);
+        for (int32_t k = 0; k < r; ++k) {
+          q[k] = (double)whead_oracle_e4m3_value(hi[k]);
+          ql[k] = (double)whead_oracle_e4m3_value(lo[k]);
+        }
+      }
 
       /* projection, base add, emitted logits, selection keys */
       for (int64_t v = 0; v < V; ++v) {
         double p = 0.0;
-        for (int32_t k = 0; k < r; ++k) p += (double)bf16_value(W[(size_t)v * r + k]) * q[k];
+        if (!fp8) {
+          for (int32_t k = 0; k < r; ++k) p += (double)bf16_value(W[(size_t)v * r + k]) * q[k];
+        } else {
+          /* p = s_w[v] (s1 sum_k Wq[v,k] hi[k] + s2 sum_k Wq[v,k] lo[k]), products and sums exact in fp64 */
+          double d1 = 0.0, d2 = 0.0;
+          for (int32_t k = 0; k < r; ++k) {
+            const double w = (double)whead_oracle_e4m3_value(Wq[(size_t)v * r + k]);
+            d1 += w * q[k];
+            d2 += w * ql[k];
+          }
+          p = (double)sw[v] * ((double)s1 * d1 + (double)s2 * d2);
+        }
         float z = (float)p + base[row_bt + (size_t)v];
         if (z_out) z_out[row_bt + (size_t)v] = z;
         if (logits) logits[row_bt + (size_t)v] = bf16_round(z);
@@ -179,6 +288,26 @@ int whead_oracle_walk(int32_t kind, int64_t V, int32_t r, const uint16_t* W, con
     }
   }
 
-  free(s); free(s_next); free(q); free(key);
+  free(s); free(s_next); free(q); free(ql); free(hi); free(lo); free(key);
   return ORACLE_OK;
+}
+
+int whead_oracle_walk(int32_t kind, int64_t V, int32_t r, const uint16_t* W, const uint16_t* E,
+                      const float* A, const float* c, const float* base, const float* s0, int32_t B,
+                      int32_t gamma, int64_t t0, float T, uint64_t seed, int32_t* tokens,
+                      uint16_t* logits, float* z_out, float* gap_out, float* state_out) {
+  return walk_impl(0, kind, V, r, W, NULL, NULL, E, A, c, base, s0, B, gamma, t0, T, seed, tokens, logits, z_out,
+                   gap_out, state_out);
+}
+
+/*
+ * The walk with E4M3 weights (Wq: V x r codes, sw: V per-row scales, from whead_oracle_quantize_w_e4m3) and
+ * the state split into two E4M3 vectors every step; every other argument and step as in whead_oracle_walk.
+ */
+int whead_oracle_walk_e4m3(int32_t kind, int64_t V, int32_t r, const uint8_t* Wq, const float* sw,
+                           const uint16_t* E, const float* A, const float* c, const float* base, const float* s0,
+                           int32_t B, int32_t gamma, int64_t t0, float T, uint64_t seed, int32_t* tokens,
+                           uint16_t* logits, float* z_out, float* gap_out, float* state_out) {
+  return walk_impl(1, kind, V, r, NULL, Wq, sw, E, A, c, base, s0, B, gamma, t0, T, seed, tokens, logits, z_out,
+                   gap_out, state_out);
 }
