@@ -277,7 +277,8 @@ def ours(args, world, rank, local):
     A = None if d["A"] is None else torch.from_numpy(d["A"]).to(dev)
     c = None if d["c"] is None else torch.from_numpy(d["c"]).to(dev)
     stream = torch.cuda.current_stream(dev)
-    head = wh.Head(W, E, kind=w["kind"], A=A, c=c, max_B=B, max_gamma=gamma, stream=stream)
+    wflags = wh.FLAG_W_E4M3 if w.get("w") == "e4m3" else 0
+    head = wh.Head(W, E, kind=w["kind"], A=A, c=c, max_B=B, max_gamma=gamma, stream=stream, flags=wflags)
     plan = head.plan(B)
     tok = torch.empty((B, gamma), dtype=torch.int32, device=dev)
     flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
@@ -414,16 +415,17 @@ def sweep(args):
     stream = torch.cuda.current_stream(dev)
     cases = []
     for name in ("markov_v4096_r64_b1_g4", "markov_v248064_r256_b1_g16", "markov_v248064_r256_b4_g16",
-                 "recurrent_v151936_r256_b1_g15"):
+                 "recurrent_v151936_r256_b1_g15", "markov_v151936_r256_b1_g16_e4m3",
+                 "markov_v248064_r256_b1_g16_e4m3", "markov_v248064_r256_b4_g16_e4m3"):
         w = I.WORKLOADS[name]
-        cases.append((name, w["kind"], w["V"], w["r"], w["B"], w["gamma"], w["T"]))
+        cases.append((name, w["kind"], w["V"], w["r"], w["B"], w["gamma"], w["T"], w.get("w", "bf16")))
     sw = I.SWEEP
     for B in sw["Bs"]:
         for g in sw["gammas"]:
             for T in sw["Ts"]:
-                cases.append((f"sweep_v{sw['V']}_b{B}_g{g}_t{int(T)}", sw["kind"], sw["V"], sw["r"], B, g, T))
+                cases.append((f"sweep_v{sw['V']}_b{B}_g{g}_t{int(T)}", sw["kind"], sw["V"], sw["r"], B, g, T, "bf16"))
     cache = {}
-    for name, kind, V, r, B, g, T in cases:
+    for name, kind, V, r, B, g, T, wfmt in cases:
         key = (kind, V, r, B, g)
         if key not in cache:
             cache.clear()
@@ -436,7 +438,8 @@ def sweep(args):
         s0 = torch.from_numpy(d["s0"]).to(dev)
         A = None if d["A"] is None else torch.from_numpy(d["A"]).to(dev)
         c = None if d["c"] is None else torch.from_numpy(d["c"]).to(dev)
-        head = wh.Head(W, E, kind=kind, A=A, c=c, max_B=B, max_gamma=g, stream=stream)
+        head = wh.Head(W, E, kind=kind, A=A, c=c, max_B=B, max_gamma=g, stream=stream,
+                       flags=wh.FLAG_W_E4M3 if wfmt == "e4m3" else 0)
         tok = torch.empty((B, g), dtype=torch.int32, device=dev)
         for _ in range(5):
             head.walk(base, s0, T=T, out_tokens=tok)
@@ -450,7 +453,7 @@ def sweep(args):
             e1.synchronize()
             ts.append(e0.elapsed_time(e1) * 1e3)
         st = head.status()
-        print(json.dumps({"case": name, "kind": "recurrent" if kind else "markov", "V": V, "r": r, "B": B,
+        print(json.dumps({"case": name, "kind": "recurrent" if kind else "markov", "w": wfmt, "V": V, "r": r, "B": B,
                           "gamma": g, "T": T, "us_per_walk": statistics.median(ts), "status": st,
                           "placement": head.plan(B)}), flush=True)
         head.close()

@@ -56,6 +56,11 @@ typedef enum { WHEAD_MARKOV = 0, WHEAD_RECURRENT = 1 } whead_kind;
                                                 memory and registers may hold; the rest are streamed. Without the
                                                 flag the planner fills shared memory, then tensor memory, then
                                                 registers, and the cap fields are ignored. */
+#define WHEAD_FLAG_W_E4M3 (1u << 4)  /* E4M3 weights (the pages' Fig. 7 two-vector projection, with the 8-bit float
+                                        format that GB300's tensor cores run fast): whead_create quantizes W into a
+                                        handle-owned copy (whead_quantize_w_e4m3), and every step splits the state
+                                        into two scaled E4M3 vectors whose projections are scaled and summed.
+                                        Requires r = 128 or 256 and max_B <= 4; not with whead_walk_noalloc. */
 #define WHEAD_FLAG_FAULT_SKIP_ARRIVAL (1u << 8) /* testing: CTA 0 never arrives at step 0's exchange, so
                                                    every other CTA's bounded wait runs out */
 
@@ -143,6 +148,15 @@ int whead_status(whead_t* h);
 
 /* The placement used for batch size B (1..max_B). */
 int whead_plan_info(const whead_t* h, int32_t B, whead_plan* out);
+
+/*
+ * E4M3 weights: quantizes W (V x r bf16, device, 16-byte aligned) row by row into Wq (V x r E4M3 codes,
+ * device, 16-byte aligned, caller-owned) and sw (V fp32 row scales, device): s = max_k |W[v,k]| / 448 (fp32),
+ * Wq[v,k] = E4M3(W[v,k] / s) rounded to nearest even and saturated at +-448; an all-zero row gets s = 0 and
+ * zero codes. Enqueued on `stream` (cudaStream_t, NULL = legacy default). r must be 128 or 256.
+ * Returns WHEAD_ERR_INVALID_ARG for null or misaligned pointers, WHEAD_ERR_UNSUPPORTED for other shapes.
+ */
+int whead_quantize_w_e4m3(const void* W, int64_t V, int32_t r, void* Wq, float* sw, void* stream);
 
 /* A static description of a return code. */
 const char* whead_strerror(int code);

@@ -211,6 +211,8 @@ static int walk_impl(int fp8, int32_t kind, int64_t V, int32_t r, const uint16_t
   uint8_t* hi = (uint8_t*)malloc((size_t)r);
   uint8_t* lo = (uint8_t*)malloc((size_t)r);
   float* key = (float*)malloc(sizeof(float) * (size_t)V);
+  double dec[256]; /* E4M3 code -> value, so the inner loop reads a table instead of decoding */
+  for (int code = 0; code < 256; ++code) dec[code] = (double)whead_oracle_e4m3_value((uint8_t)code);
   if (!s || !s_next || !q || !ql || !hi || !lo || !key) {
     free(s); free(s_next); free(q); free(ql); free(hi); free(lo); free(key);
     return ORACLE_ENOMEM;
@@ -244,7 +246,7 @@ static int walk_impl(int fp8, int32_t kind, int64_t V, int32_t r, const uint16_t
           /* p = s_w[v] (s1 sum_k Wq[v,k] hi[k] + s2 sum_k Wq[v,k] lo[k]), products and sums exact in fp64 */
           double d1 = 0.0, d2 = 0.0;
           for (int32_t k = 0; k < r; ++k) {
-            const double w = (double)whead_oracle_e4m3_value(Wq[(size_t)v * r + k]);
+            const double w = dec[Wq[(size_t)v * r + k]];
             d1 += w * q[k];
             d2 += w * ql[k];
           }

@@ -31,6 +31,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <type_traits>
@@ -57,7 +58,8 @@ constexpr uint32_t kFlagForceStream = 1u << 2;
 constexpr uint32_t kFlagSkipArrival = 1u << 8;
 
 struct WalkArgs {
-  const uint16_t* W;
+  const uint16_t* W;  // rows of rw 16-bit words: bf16 values, or (E4M3 weights) pairs of 8-bit codes
+  const float* sw;    // E4M3 weights: one fp32 scale per row of W; null otherwise
   const uint16_t* E;
   const float* A;
   const float* c;
@@ -81,6 +83,7 @@ struct WalkArgs {
   uint64_t timeout_ns;
   float T;
   int32_t r;
+  int32_t rw;        // length of a row of W in 16-bit words: r, or r / 2 for E4M3 codes
   int32_t B;
   int32_t gamma;
   int32_t kind;
@@ -106,8 +109,9 @@ __host__ __device__ constexpr uint32_t wl_entry(int j, uint32_t tier, int col) {
 
 // Shared-memory layout after the W tier (byte offsets from the 1024-aligned base).
 struct SmemLayout {
-  int red, win, misc, base, h, a, total;
-  __host__ __device__ static SmemLayout make(int smem_w_bytes, int B, int r, int ra, bool recurrent, int ng) {
+  int red, win, misc, base, h, a, sw, total;
+  __host__ __device__ static SmemLayout make(int smem_w_bytes, int B, int r, int ra, bool recurrent, int ng,
+                                             bool f8 = false) {
     SmemLayout L;
     L.red = smem_w_bytes;                       // [kWarps][kMaxB] u64
     L.win = L.red + kWarps * kMaxB * 8;         // [kMaxB] int32
@@ -115,7 +119,8 @@ struct SmemLayout {
     L.base = L.misc + 16;                       // [B][ng * 16] fp32: this step's base logits of the CTA's rows
     L.h = L.base + B * ng * kGroupRows * 4;     // recurrent: [B][r] fp32
     L.a = L.h + (recurrent ? B * r * 4 : 0);    // recurrent: [ra][r] fp32
-    L.total = L.a + (recurrent ? ra * r * 4 : 0);
+    L.sw = L.a + (recurrent ? ra * r * 4 : 0);  // E4M3 weights: [ng * 16] fp32 row scales
+    L.total = L.sw + (f8 ? ng * kGroupRows * 4 : 0);
     return L;
   }
 };
@@ -157,6 +162,22 @@ __device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint3
 __device__ __forceinline__ void mma_bf16_16816_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                                  uint32_t b0, uint32_t b1) {
   asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+// E4M3 x E4M3 -> fp32, 16 x 8 x 32. Its fragments have the bf16 16 x 8 x 16 layout byte for byte (each 32-bit
+// register holds four 8-bit values where the bf16 layout holds two 16-bit ones), so the same storage orders
+// serve both formats.
+__device__ __forceinline__ void mma_e4m3_16832(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_e4m3_16832_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                                 uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k32.row.col.f32.e4m3.e4m3.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
 }
@@ -314,19 +335,116 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // The four ops of a box go to four independent accumulators so that they issue back to back. The box's
 // A operands are stored in fragment order: a[4m .. 4m + 3] = {a0, a1, a2, a3} of op m (m = 2 rho + h), so
 // each op reads four consecutive registers as they were loaded.
-template <int KB, int NH>
+template <int KB, int NH, bool F8 = false>
 __device__ __forceinline__ void mma_box(float (&acc)[4][NH][4], const uint32_t (&a)[16],
                                         const uint32_t (&bf)[NH][KB][8], int bx) {
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
 #pragma unroll
     for (int n = 0; n < NH; ++n) {
-      if (bx == 0)
-        mma_bf16_16816_z(acc[m][n], a[4 * m], a[4 * m + 1], a[4 * m + 2], a[4 * m + 3], bf[n][bx][2 * m],
+      if constexpr (F8) {
+        if (bx == 0)
+          mma_e4m3_16832_z(acc[m][n], a[4 * m], a[4 * m + 1], a[4 * m + 2], a[4 * m + 3], bf[n][bx][2 * m],
+                           bf[n][bx][2 * m + 1]);
+        else
+          mma_e4m3_16832(acc[m][n], a[4 * m], a[4 * m + 1], a[4 * m + 2], a[4 * m + 3], bf[n][bx][2 * m],
                          bf[n][bx][2 * m + 1]);
-      else
-        mma_bf16_16816(acc[m][n], a[4 * m], a[4 * m + 1], a[4 * m + 2], a[4 * m + 3], bf[n][bx][2 * m],
-                       bf[n][bx][2 * m + 1]);
+      } else {
+        if (bx == 0)
+          mma_bf16_16816_z(acc[m][n], a[4 * m], a[4 * m + 1], a[4 * m + 2], a[4 * m + 3], bf[n][bx][2 * m],
+                           bf[n][bx][2 * m + 1]);
+        else
+          mma_bf16_16816(acc[m][n], a[4 * m], a[4 * m + 1], a[4 * m + 2], a[4 * m + 3], bf[n][bx][2 * m],
+                         bf[n][bx][2 * m + 1]);
+      }
+    }
+  }
+}
+
+// ---- E4M3 weights: the state as two scaled E4M3 vectors -----------------------------------------------------
+// (Fig. 7 of the pages represents u by two 8-bit vectors whose scaled projections are summed.)
+
+// Four fp32 values to four E4M3 codes (round to nearest even, saturating at +-448), first value in byte 0.
+__device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
+  const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return lo | (hi << 16);
+}
+
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+  return __half2float(__half(__nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)code, __NV_E4M3)));
+}
+
+// Largest |x| over the warp (non-negative floats order as their bit patterns), every lane gets it.
+__device__ __forceinline__ float warp_absmax(float m) {
+  uint32_t b = __float_as_uint(fabsf(m)), r;
+  asm volatile("redux.sync.max.u32 %0, %1, 0xffffffff;" : "=r"(r) : "r"(b));
+  return __uint_as_float(r);
+}
+
+// Quantizes a vector spread over the warp (lane L holds elements [L * EPL, L * EPL + EPL)): scale
+// s = max|x| / 448, codes E4M3(x / s) packed four to a word, or s = 0 and zero codes for an all-zero vector.
+template <int EPL>
+__device__ __forceinline__ float quantize_e4m3_warp(const float (&x)[EPL], uint32_t (&q)[EPL / 4]) {
+  const float amax = [&] {
+    float m = 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) m = fmaxf(m, fabsf(x[e]));
+    return warp_absmax(m);
+  }();
+  const float s = amax == 0.f ? 0.f : __fdiv_rn(amax, 448.f);
+#pragma unroll
+  for (int w = 0; w < EPL / 4; ++w)
+    q[w] = s == 0.f ? 0u
+                    : e4m3x4(__fdiv_rn(x[4 * w], s), __fdiv_rn(x[4 * w + 1], s), __fdiv_rn(x[4 * w + 2], s),
+                             __fdiv_rn(x[4 * w + 3], s));
+  return s;
+}
+
+// B fragments of the E4M3 projection for B <= 4 walks: column 2w holds walk w's hi vector, column 2w + 1 its
+// lo vector (the residual). load(w, x) puts walk w's state elements [lane * EPL, lane * EPL + EPL) in x. The
+// fragment word i of box bx of lane (g, c) is state bytes 128 bx + 32 c + 4 i (the same order as the bf16
+// path's), gathered by shuffles from the lane that quantized them. s1c / s2c: the scales of walk c (the
+// walk whose sums this lane's accumulator columns 2c, 2c + 1 hold). Every lane of the warp must call this.
+template <int KB, typename Load>
+__device__ __forceinline__ void bfrag_e4m3(uint32_t (&bf)[1][KB][8], float& s1c, float& s2c, int B, int lane,
+                                           Load load) {
+  constexpr int EPL = 4 * KB;  // r = 128 KB elements over 32 lanes
+  const int g = lane >> 2, c = lane & 3;
+#pragma unroll
+  for (int bx = 0; bx < KB; ++bx)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) bf[0][bx][i] = 0u;
+  s1c = 0.f;
+  s2c = 0.f;
+#pragma unroll
+  for (int w = 0; w < 4; ++w) {
+    if (w >= B) break;
+    float x[EPL];
+    load(w, x);
+    uint32_t qh[KB], ql[KB];
+    const float s1 = quantize_e4m3_warp<EPL>(x, qh);
+    float res[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) {
+      const uint32_t code = (qh[e / 4] >> (8 * (e % 4))) & 0xFFu;
+      res[e] = __fsub_rn(x[e], __fmul_rn(s1, e4m3_value(code)));
+    }
+    const float s2 = quantize_e4m3_warp<EPL>(res, ql);
+#pragma unroll
+    for (int bx = 0; bx < KB; ++bx)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int o = 128 * bx + 32 * c + 4 * i;  // state byte (= element) offset of this fragment word
+        // 128 bx and 32 c are multiples of EPL (4 or 8), so the word within the source lane depends on i only
+        const int src = o / EPL, wi = ((4 * i) % EPL) / 4;
+        const uint32_t h = __shfl_sync(0xffffffffu, qh[wi], src);
+        const uint32_t l = __shfl_sync(0xffffffffu, ql[wi], src);
+        if ((g >> 1) == w) bf[0][bx][i] = (g & 1) ? l : h;
+      }
+    if (c == w) {
+      s1c = s1;
+      s2c = s2;
     }
   }
 }
@@ -436,7 +554,7 @@ __device__ __forceinline__ void stage_base(const WalkArgs& P, float* s_base, int
 // Warp roles: warps in rf_warp_mask keep one group in registers (plus shared-memory groups); the others
 // own the tensor-memory groups of their lane quadrant (plus shared-memory groups). The two roles run
 // separately compiled copies of the step loop so that neither pays for the other's registers.
-template <int KB, int NH, bool NB1>
+template <int KB, int NH, bool NB1, bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     walk_kernel(const __grid_constant__ CUtensorMap tmapW, const __grid_constant__ CUtensorMap tmapW128,
                 const __grid_constant__ WalkArgs P) {
@@ -450,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
-  const SmemLayout L = SmemLayout::make(P.smem_w_bytes, B, r, P.ra, recurrent, P.ng);
+  const SmemLayout L = SmemLayout::make(P.smem_w_bytes, B, r, P.ra, recurrent, P.ng, F8);
   uint8_t* sW = smem;
   unsigned long long* s_red = reinterpret_cast<unsigned long long*>(smem + L.red);
   int32_t* s_win = reinterpret_cast<int32_t*>(smem + L.win);
@@ -460,6 +578,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* s_base = reinterpret_cast<float*>(smem + L.base);
   float* s_h = reinterpret_cast<float*>(smem + L.h);
   float* s_A = reinterpret_cast<float*>(smem + L.a);
+  float* s_sw = reinterpret_cast<float*>(smem + L.sw);  // E4M3 weights: scales of this CTA's rows
+  static_assert(!F8 || NH == 1, "E4M3 weights take two accumulator columns per walk: at most 4 walks");
 
   const uint32_t mbar = smem_u32(s_mbar);
   trace_stamp(P, 0);
@@ -534,7 +654,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int64_t v0 = row_base + (int64_t)kGroupRows * j + g;
       uint32_t a[KB][16];
 #pragma unroll
-      for (int bx = 0; bx < KB; ++bx) load_box_global(a[bx], P.W, v0, V, r, bx, c);
+      for (int bx = 0; bx < KB; ++bx) load_box_global(a[bx], P.W, v0, V, P.rw, bx, c);
 #pragma unroll
       for (int bx = 0; bx < KB; ++bx) {
         uint32_t q[16];
@@ -548,12 +668,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int e = 0; e < my_count; ++e) {
     const uint32_t ent = __shfl_sync(0xffffffffu, my_entry, e);
     if (((ent >> 8) & 3u) != kTierStream) continue;
-    // the group's 16 rows are 32 r contiguous bytes: one prefetch per 128-byte line, rows below V only
+    // the group's 16 rows are 32 rw contiguous bytes: one prefetch per 128-byte line, rows below V only
     const int64_t v0 = row_base + (int64_t)kGroupRows * (int)(ent & 0xFFu);
-    const uint8_t* gb = reinterpret_cast<const uint8_t*>(P.W + v0 * r);
-    for (int L = lane; L < r / 4; L += 32)
-      if (v0 + (L * 128) / (2 * r) < V) prefetch_l2(gb + L * 128);
+    const uint8_t* gb = reinterpret_cast<const uint8_t*>(P.W + v0 * P.rw);
+    for (int L = lane; L < P.rw / 4; L += 32)
+      if (v0 + (L * 128) / (2 * P.rw) < V) prefetch_l2(gb + L * 128);
   }
+
+  // E4M3 weights: the row scales of this CTA's rows (rows past V read as zero)
+  if constexpr (F8)
+    for (int lr = tid; lr < rows_cta; lr += kThreads) s_sw[lr] = (row_base + lr < V) ? P.sw[row_base + lr] : 0.f;
 
   // recurrent head: the initial state and this CTA's rows of A
   const int a_lo = cta * P.ra;
@@ -618,7 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int bx = 0; bx < KB; ++bx) {
         if (jr >= 0) {
           uint32_t a[16];
-          load_box_global(a, P.W, row_base + (int64_t)kGroupRows * jr + g, V, r, bx, c);
+          load_box_global(a, P.W, row_base + (int64_t)kGroupRows * jr + g, V, P.rw, bx, c);
           rows_to_fragments(rfA[bx], a);
         } else {
 #pragma unroll
@@ -628,16 +752,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     uint32_t bf[NH][KB][8];
+    // E4M3 weights: the scales of walk c's two state vectors (this lane's accumulator columns 2c, 2c + 1)
+    float es1 = 0.f, es2 = 0.f;
+    // the state of walk w as fp32 (initial state, or the recurrent state in shared memory)
+    auto load_f32_state = [&](int w, auto& x) {
+      const float* src = (recurrent ? s_h : P.s0) + (int64_t)w * r + lane * 4 * KB;
 #pragma unroll
-    for (int h = 0; h < NH; ++h) {
-      const int n = 8 * h + g;
-      if (n < B) {
-        bfrag_from_f32<KB>(bf[h], recurrent ? (s_h + n * r) : (P.s0 + (int64_t)n * r), c);
-      } else {
+      for (int e = 0; e < 4 * KB; ++e) x[e] = src[e];
+    };
+    if constexpr (F8) {
+      bfrag_e4m3<KB>(bf, es1, es2, B, lane, load_f32_state);
+    } else {
 #pragma unroll
-        for (int bx = 0; bx < KB; ++bx)
+      for (int h = 0; h < NH; ++h) {
+        const int n = 8 * h + g;
+        if (n < B) {
+          bfrag_from_f32<KB>(bf[h], recurrent ? (s_h + n * r) : (P.s0 + (int64_t)n * r), c);
+        } else {
 #pragma unroll
-          for (int i = 0; i < 8; ++i) bf[h][bx][i] = 0u;
+          for (int bx = 0; bx < KB; ++bx)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) bf[h][bx][i] = 0u;
+        }
       }
     }
 
@@ -687,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               const uint4 x = *reinterpret_cast<const uint4*>(p + bx * box_stride + m * 512);
               a[4 * m] = x.x; a[4 * m + 1] = x.y; a[4 * m + 2] = x.z; a[4 * m + 3] = x.w;
             }
-            mma_box<KB, NH>(acc, a, bf, bx);
+            mma_box<KB, NH, F8>(acc, a, bf, bx);
           }
         } else if (tier == kTierTmem) {
           if constexpr (!RFW) {
@@ -697,11 +833,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               tmem_ld32(a0, taddr);
               tmem_wait_ld_boxes<2>(a0);
               tmem_ld32(a1, taddr + 32);
-              mma_box<KB, NH>(acc, a0[0], bf, 0);
-              mma_box<KB, NH>(acc, a0[1], bf, 1);
+              mma_box<KB, NH, F8>(acc, a0[0], bf, 0);
+              mma_box<KB, NH, F8>(acc, a0[1], bf, 1);
               tmem_wait_ld_boxes<2>(a1);
-              mma_box<KB, NH>(acc, a1[0], bf, 2);
-              mma_box<KB, NH>(acc, a1[1], bf, 3);
+              mma_box<KB, NH, F8>(acc, a1[0], bf, 2);
+              mma_box<KB, NH, F8>(acc, a1[1], bf, 3);
             } else {
               // boxes read per wait: all of them for one batch half, two when both halves are live
               constexpr int TB = (NH == 1 || KB < 4) ? KB : 2;
@@ -712,7 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int i = 0; i < TB; ++i) tmem_ld16(a[i], taddr + 16 * (b0 + i));
                 tmem_wait_ld_boxes<TB>(a);
 #pragma unroll
-                for (int i = 0; i < TB; ++i) mma_box<KB, NH>(acc, a[i], bf, b0 + i);
+                for (int i = 0; i < TB; ++i) mma_box<KB, NH, F8>(acc, a[i], bf, b0 + i);
               }
             }
           } else {
@@ -732,14 +868,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int b0 = 0; b0 < KB; b0 += SB) {
             uint32_t a[SB][16];
 #pragma unroll
-            for (int i = 0; i < SB; ++i) load_box_global_frag(a[i], P.W, v0, V, r, b0 + i, c);
+            for (int i = 0; i < SB; ++i) load_box_global_frag(a[i], P.W, v0, V, P.rw, b0 + i, c);
 #pragma unroll
-            for (int i = 0; i < SB; ++i) mma_box<KB, NH>(acc, a[i], bf, b0 + i);
+            for (int i = 0; i < SB; ++i) mma_box<KB, NH, F8>(acc, a[i], bf, b0 + i);
           }
         } else {
           if constexpr (RFW) {
 #pragma unroll
-            for (int bx = 0; bx < KB; ++bx) mma_box<KB, NH>(acc, rfA[bx], bf, bx);
+            for (int bx = 0; bx < KB; ++bx) mma_box<KB, NH, F8>(acc, rfA[bx], bf, bx);
           } else {
 #pragma unroll
             for (int s = 0; s < 4; ++s)
@@ -753,7 +889,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         // z = p + base: each (row, walk) of the group belongs to one lane, which adds its projection to
         // the staged base logit in place (Fig. 7: projection summed, then added to the base logits)
         const int lr0 = kGroupRows * j + g;
-        if constexpr (NB1) {
+        if constexpr (F8) {
+          // E4M3 weights: columns 2c and 2c + 1 hold walk c's sums over its hi and lo vectors;
+          // p = s_w (s1 sum_hi + s2 sum_lo)
+          if (c < B) {
+            const float h0 = __fadd_rn(__fadd_rn(acc[0][0][0], acc[1][0][0]), __fadd_rn(acc[2][0][0], acc[3][0][0]));
+            const float l0 = __fadd_rn(__fadd_rn(acc[0][0][1], acc[1][0][1]), __fadd_rn(acc[2][0][1], acc[3][0][1]));
+            const float h1 = __fadd_rn(__fadd_rn(acc[0][0][2], acc[1][0][2]), __fadd_rn(acc[2][0][2], acc[3][0][2]));
+            const float l1 = __fadd_rn(__fadd_rn(acc[0][0][3], acc[1][0][3]), __fadd_rn(acc[2][0][3], acc[3][0][3]));
+            const float p0 = __fmul_rn(s_sw[lr0], __fadd_rn(__fmul_rn(es1, h0), __fmul_rn(es2, l0)));
+            const float p1 = __fmul_rn(s_sw[lr0 + 8], __fadd_rn(__fmul_rn(es1, h1), __fmul_rn(es2, l1)));
+            float* zr = s_base + c * rows_cta + lr0;
+            if constexpr (NB1) {
+              zr[0] = __fadd_rn(p0, zb0);
+              zr[8] = __fadd_rn(p1, zb1);
+            } else {
+              zr[0] = __fadd_rn(p0, zr[0]);
+              zr[8] = __fadd_rn(p1, zr[8]);
+            }
+          }
+        } else if constexpr (NB1) {
           if (c == 0) {
             s_base[lr0] = __fadd_rn(__fadd_rn(__fadd_rn(acc[0][0][0], acc[1][0][0]), __fadd_rn(acc[2][0][0], acc[3][0][0])),
                                     zb0);
@@ -977,10 +1132,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------- state advance ----------------
       if (P.flags & kFlagFixedLatent) continue;
       if (!recurrent) {
+        if constexpr (F8) {
+          // the winners' E rows, split into two E4M3 vectors by every warp
+          bfrag_e4m3<KB>(bf, es1, es2, B, lane, [&](int w, auto& x) {
+            const uint16_t* er = P.E + (int64_t)s_win[w] * r + lane * 4 * KB;
+            uint32_t u[2 * KB];
+            if constexpr (KB == 2) {
+              const uint4 v = __ldg(reinterpret_cast<const uint4*>(er));
+              u[0] = v.x; u[1] = v.y; u[2] = v.z; u[3] = v.w;
+            } else {
+              const uint2 v = __ldg(reinterpret_cast<const uint2*>(er));
+              u[0] = v.x; u[1] = v.y;
+            }
 #pragma unroll
-        for (int h = 0; h < NH; ++h) {
-          const int n = 8 * h + g;
-          if (n < B) bfrag_from_bf16_row<KB>(bf[h], P.E + (int64_t)s_win[n] * r, c);
+            for (int e = 0; e < 2 * KB; ++e) {
+              x[2 * e] = __uint_as_float(u[e] << 16);
+              x[2 * e + 1] = __uint_as_float(u[e] & 0xFFFF0000u);
+            }
+          });
+        } else {
+#pragma unroll
+          for (int h = 0; h < NH; ++h) {
+            const int n = 8 * h + g;
+            if (n < B) bfrag_from_bf16_row<KB>(bf[h], P.E + (int64_t)s_win[n] * r, c);
+          }
         }
         if (cta == 0 && P.state) {
           for (int i = tid; i < B * r; i += kThreads) {
@@ -999,10 +1174,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           s_h[i] = tanhf(pre);
         }
         __syncthreads();
+        if constexpr (F8) {
+          bfrag_e4m3<KB>(bf, es1, es2, B, lane, load_f32_state);
+        } else {
 #pragma unroll
-        for (int h = 0; h < NH; ++h) {
-          const int n = 8 * h + g;
-          if (n < B) bfrag_from_f32<KB>(bf[h], s_h + n * r, c);
+          for (int h = 0; h < NH; ++h) {
+            const int n = 8 * h + g;
+            if (n < B) bfrag_from_f32<KB>(bf[h], s_h + n * r, c);
+          }
         }
         if (cta == 0 && P.state) {
           for (int i = tid; i < B * r; i += kThreads) {

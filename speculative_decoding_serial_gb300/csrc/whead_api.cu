@@ -43,6 +43,9 @@ struct whead_s {
   whead_params p{};
   const uint16_t* W = nullptr;
   const uint16_t* E = nullptr;
+  bool f8 = false;         // E4M3 weights: the handle's quantized copy of W and its row scales
+  uint8_t* wq = nullptr;   // V x r E4M3 codes
+  float* sw = nullptr;     // V row scales
   CUtensorMap tmap{};     // W: 64 x 16 boxes
   CUtensorMap tmap128{};  // W: 64 x 128 boxes
   int sm_count = 0, smem_optin = 0;
@@ -62,17 +65,19 @@ struct whead_s {
 
 namespace {
 
-int kb_of(int r) { return r / 64; }
+// 128-byte boxes per row of W: 64 bf16 values, or 128 E4M3 codes
+int kb_of(int r, bool f8 = false) { return f8 ? r / 128 : r / 64; }
 
 // Planner: number of CTAs, groups per CTA and their tier; per-warp work lists balanced over the four
 // SM sub-partitions (warp % 4), which each own one tensor core and one quarter of tensor memory.
 // cap_*: most groups per CTA a tier may take (INT_MAX: as many as fit). fixed_tiers: the caps come from the
 // caller (a measurement mode), so the grid is all SMs (or grid_req) and the groups past the caps are streamed.
 Plan make_plan(int64_t V, int r, int kind, int Bcap, int NH, int sm_count, int smem_optin, int grid_req,
-               int cap_smem = INT_MAX, int cap_tmem = INT_MAX, int cap_rf = INT_MAX, bool fixed_tiers = false) {
+               int cap_smem = INT_MAX, int cap_tmem = INT_MAX, int cap_rf = INT_MAX, bool fixed_tiers = false,
+               bool f8 = false) {
   Plan P;
   sm_count = std::min(sm_count, kMaxGrid);
-  const int KB = kb_of(r);
+  const int KB = kb_of(r, f8);
   const int64_t ngt = (V + kGroupRows - 1) / kGroupRows;
   const int64_t group_bytes = (int64_t)KB * kBoxBytes;
   const bool recurrent = kind == WHEAD_RECURRENT;
@@ -84,7 +89,7 @@ Plan make_plan(int64_t V, int r, int kind, int Bcap, int NH, int sm_count, int s
     if (ng64 > 255) return false;
     const int ng = (int)ng64;
     const int ra = recurrent ? (r + G - 1) / G : 0;
-    const SmemLayout L0 = SmemLayout::make(0, Bcap, r, ra, recurrent, ng);
+    const SmemLayout L0 = SmemLayout::make(0, Bcap, r, ra, recurrent, ng, f8);
     const int64_t fixed = 1024 + L0.total;
     const int64_t smem_groups_max = std::min<int64_t>(cap_smem, std::max<int64_t>(0, (smem_optin - fixed) / group_bytes));
     int n_smem = (int)std::min<int64_t>(ng, smem_groups_max);
@@ -105,7 +110,7 @@ Plan make_plan(int64_t V, int r, int kind, int Bcap, int NH, int sm_count, int s
     out.ra = ra;
     out.Bcap = Bcap;
     out.smem_w_bytes = (int)(n_smem * group_bytes);
-    out.smem_bytes = (int)(1024 + SmemLayout::make(out.smem_w_bytes, Bcap, r, ra, recurrent, ng).total);
+    out.smem_bytes = (int)(1024 + SmemLayout::make(out.smem_w_bytes, Bcap, r, ra, recurrent, ng, f8).total);
     if (n_tmem > 0) {
       const int cols = ((n_tmem - 1) / 4 + 1) * 16 * KB;
       uint32_t pw = 32;
@@ -194,9 +199,9 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-template <int KB, int NH, bool NB1>
+template <int KB, int NH, bool NB1, bool F8 = false>
 int launch_t(whead_t* h, const Plan& pl, const WalkArgs& a) {
-  auto fn = walk_kernel<KB, NH, NB1>;
+  auto fn = walk_kernel<KB, NH, NB1, F8>;
   static int attr_bytes = 0;  // largest dynamic shared memory size granted so far (per instantiation)
   if (pl.smem_bytes > attr_bytes) {
     if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, h->smem_optin) != cudaSuccess)
@@ -219,8 +224,17 @@ int launch_t(whead_t* h, const Plan& pl, const WalkArgs& a) {
 
 // Instantiation for (rank boxes, batch halves, single walk).
 int launch(whead_t* h, const Plan& pl, const WalkArgs& a, int NH) {
-  const int KB = kb_of(h->p.r);
   const bool one = a.B == 1;
+  if (h->f8) {  // E4M3 weights: one batch half (at most 4 walks), r = 128 or 256
+    switch (kb_of(h->p.r, true) * 2 + (one ? 1 : 0)) {
+      case 2: return launch_t<1, 1, false, true>(h, pl, a);
+      case 3: return launch_t<1, 1, true, true>(h, pl, a);
+      case 4: return launch_t<2, 1, false, true>(h, pl, a);
+      case 5: return launch_t<2, 1, true, true>(h, pl, a);
+      default: return WHEAD_ERR_UNSUPPORTED;
+    }
+  }
+  const int KB = kb_of(h->p.r);
   switch (KB * 4 + (NH - 1) * 2 + (one ? 1 : 0)) {
     case 4: return launch_t<1, 1, false>(h, pl, a);
     case 5: return launch_t<1, 1, true>(h, pl, a);
@@ -240,6 +254,37 @@ int launch(whead_t* h, const Plan& pl, const WalkArgs& a, int NH) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// E4M3 weights: one warp per row quantizes it as a vector (scale max|w| / 448, codes E4M3(w / s)) with the
+// same warp routine the walk uses for its state. EPL = r / 32 elements per lane.
+template <int EPL>
+__global__ void quantize_w_e4m3_kernel(const uint16_t* __restrict__ W, int64_t V, int r, uint8_t* __restrict__ Wq,
+                                       float* __restrict__ sw) {
+  const int lane = threadIdx.x & 31;
+  const int64_t v = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+  if (v >= V) return;  // the same for every lane of the warp
+  const uint16_t* row = W + v * r + lane * EPL;
+  uint32_t u[EPL / 2];
+  if constexpr (EPL == 8) {
+    const uint4 t = *reinterpret_cast<const uint4*>(row);
+    u[0] = t.x; u[1] = t.y; u[2] = t.z; u[3] = t.w;
+  } else {
+    const uint2 t = *reinterpret_cast<const uint2*>(row);
+    u[0] = t.x; u[1] = t.y;
+  }
+  float x[EPL];
+#pragma unroll
+  for (int e = 0; e < EPL / 2; ++e) {
+    x[2 * e] = __uint_as_float(u[e] << 16);
+    x[2 * e + 1] = __uint_as_float(u[e] & 0xFFFF0000u);
+  }
+  uint32_t q[EPL / 4];
+  const float s = quantize_e4m3_warp<EPL>(x, q);
+  uint32_t* dst = reinterpret_cast<uint32_t*>(Wq + v * r + lane * EPL);
+#pragma unroll
+  for (int w = 0; w < EPL / 4; ++w) dst[w] = q[w];
+  if (lane == 0) sw[v] = s;
+}
+
 // TMA descriptor of W (2-D: r elements inner, V rows) with 64-element x `rows` boxes, 128-byte swizzle and
 // zero fill outside the tensor.
 int encode_w(CUtensorMap* m, const void* W, int64_t V, int r, int rows) {
@@ -258,6 +303,20 @@ int encode_w(CUtensorMap* m, const void* W, int64_t V, int r, int rows) {
 }  // namespace
 
 extern "C" {
+
+int whead_quantize_w_e4m3(const void* W, int64_t V, int32_t r, void* Wq, float* sw, void* stream) {
+  if (!W || !Wq || !sw || V < 1) return WHEAD_ERR_INVALID_ARG;
+  if (r != 128 && r != 256) return WHEAD_ERR_UNSUPPORTED;
+  if (V >= (int64_t)1 << 24) return WHEAD_ERR_UNSUPPORTED;
+  if (!aligned16(W) || !aligned16(Wq) || (reinterpret_cast<uintptr_t>(sw) & 3u)) return WHEAD_ERR_INVALID_ARG;
+  const unsigned blocks = (unsigned)((V + 7) / 8);  // 8 rows (warps) per block
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const uint16_t* w = static_cast<const uint16_t*>(W);
+  uint8_t* q = static_cast<uint8_t*>(Wq);
+  if (r == 256) quantize_w_e4m3_kernel<8><<<blocks, 256, 0, s>>>(w, V, r, q, sw);
+  else quantize_w_e4m3_kernel<4><<<blocks, 256, 0, s>>>(w, V, r, q, sw);
+  return cudaGetLastError() == cudaSuccess ? WHEAD_OK : WHEAD_ERR_CUDA;
+}
 
 const char* whead_strerror(int code) {
   switch (code) {
@@ -283,12 +342,15 @@ int whead_create(const void* W, const void* E, const whead_params* params, whead
   if (p.r != 64 && p.r != 128 && p.r != 192 && p.r != 256) return WHEAD_ERR_UNSUPPORTED;
   if (p.kind == WHEAD_RECURRENT && !p.A) return WHEAD_ERR_UNSUPPORTED;
   if (!aligned16(W) || !aligned16(E)) return WHEAD_ERR_INVALID_ARG;
+  const bool f8 = (p.flags & WHEAD_FLAG_W_E4M3) != 0u;
+  if (f8 && ((p.r != 128 && p.r != 256) || p.max_B > 4)) return WHEAD_ERR_UNSUPPORTED;
 
   whead_t* h = new (std::nothrow) whead_s();
   if (!h) return WHEAD_ERR_INVALID_ARG;
   h->p = p;
   h->W = static_cast<const uint16_t*>(W);
   h->E = static_cast<const uint16_t*>(E);
+  h->f8 = f8;
   h->stream = static_cast<cudaStream_t>(p.stream);
   if (h->p.timeout_us == 0) h->p.timeout_us = 1000000u;
   auto fail = [&](int code) {
@@ -321,7 +383,7 @@ int whead_create(const void* W, const void* E, const whead_params* params, whead
   }
   const bool fixed = force_stream || capped;
   h->plan[0] = make_plan(p.V, p.r, p.kind, std::min(p.max_B, 8), 1, h->sm_count, h->smem_optin, p.grid, cap_s, cap_t,
-                         cap_r, fixed);
+                         cap_r, fixed, f8);
   if (!h->plan[0].ok) return fail(WHEAD_ERR_UNSUPPORTED);
   if (p.max_B > 8) {
     h->plan[1] = make_plan(p.V, p.r, p.kind, p.max_B, 2, h->sm_count, h->smem_optin, p.grid, cap_s, cap_t, cap_r,
@@ -329,9 +391,21 @@ int whead_create(const void* W, const void* E, const whead_params* params, whead
     if (!h->plan[1].ok) return fail(WHEAD_ERR_UNSUPPORTED);
   }
 
-  // TMA descriptors of W: 64 x 16 and 64 x 128 boxes
-  if (encode_w(&h->tmap, W, p.V, p.r, kGroupRows) != WHEAD_OK) return fail(WHEAD_ERR_CUDA);
-  if (encode_w(&h->tmap128, W, p.V, p.r, kGroupRows * kTmaChunkGroups) != WHEAD_OK) return fail(WHEAD_ERR_CUDA);
+  // E4M3 weights: the handle quantizes W once into its own copy (codes and row scales)
+  const void* Wt = W;
+  int rw = p.r;
+  if (f8) {
+    if (cudaMalloc(&h->wq, (size_t)p.V * p.r) != cudaSuccess) return fail(WHEAD_ERR_CUDA);
+    if (cudaMalloc(&h->sw, (size_t)p.V * 4) != cudaSuccess) return fail(WHEAD_ERR_CUDA);
+    const int rc = whead_quantize_w_e4m3(W, p.V, p.r, h->wq, h->sw, h->stream);
+    if (rc != WHEAD_OK) return fail(rc);
+    Wt = h->wq;
+    rw = p.r / 2;  // the codes, described to TMA as pairs: rows of r / 2 16-bit words
+  }
+
+  // TMA descriptors of W: 64 x 16 and 64 x 128 boxes of 16-bit words
+  if (encode_w(&h->tmap, Wt, p.V, rw, kGroupRows) != WHEAD_OK) return fail(WHEAD_ERR_CUDA);
+  if (encode_w(&h->tmap128, Wt, p.V, rw, kGroupRows * kTmaChunkGroups) != WHEAD_OK) return fail(WHEAD_ERR_CUDA);
 
   // scratch: exchange slots (two call parities), two counters on their own lines, A h slices, status word
   const size_t slots_bytes = 2 * (size_t)h->slots_per_parity * 8;
@@ -361,7 +435,9 @@ int whead_walk_ex(whead_t* h, const float* base, const float* s0, int32_t B, int
 
   WalkArgs a;
   std::memset(&a, 0, sizeof(a));
-  a.W = h->W;
+  a.W = h->f8 ? reinterpret_cast<const uint16_t*>(h->wq) : h->W;
+  a.sw = h->f8 ? h->sw : nullptr;
+  a.rw = h->f8 ? h->p.r / 2 : h->p.r;
   a.E = h->E;
   a.A = h->p.A;
   a.c = h->p.c;
@@ -488,6 +564,8 @@ int whead_destroy(whead_t* h) {
     if (cudaStreamSynchronize(h->stream) != cudaSuccess) rc = WHEAD_ERR_CUDA;
   }
   if (h->scratch_block) cudaFree(h->scratch_block);
+  if (h->wq) cudaFree(h->wq);
+  if (h->sw) cudaFree(h->sw);
   if (h->d_base) cudaFree(h->d_base);
   if (h->d_u0) cudaFree(h->d_u0);
   if (h->d_tok) cudaFree(h->d_tok);
@@ -546,7 +624,7 @@ int noalloc_setup(int dev, NaDevice** out) {
 template <int KB, int NH, bool NB1>
 int noalloc_launch_t(const CUtensorMap& tmap, const CUtensorMap& tmap128, cudaStream_t stream, int smem_optin,
                      const Plan& pl, const WalkArgs& a) {
-  auto fn = walk_kernel<KB, NH, NB1>;
+  auto fn = walk_kernel<KB, NH, NB1, false>;
   if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin) != cudaSuccess)
     return WHEAD_ERR_CUDA;
   void* args[] = {(void*)&tmap, (void*)&tmap128, (void*)&a};
@@ -595,6 +673,7 @@ extern "C" int whead_walk_noalloc(const void* W, const void* E, const whead_para
   if (p.V >= (int64_t)1 << 24) return WHEAD_ERR_UNSUPPORTED;
   if (p.r != 64 && p.r != 128 && p.r != 192 && p.r != 256) return WHEAD_ERR_UNSUPPORTED;
   if (p.kind == WHEAD_RECURRENT && !p.A) return WHEAD_ERR_UNSUPPORTED;
+  if (p.flags & WHEAD_FLAG_W_E4M3) return WHEAD_ERR_UNSUPPORTED;  // needs the handle's quantized copy of W
   if (!(T >= 0.0f) || T > 3.0e38f) return WHEAD_ERR_INVALID_ARG;
   if (!aligned16(W) || !aligned16(E) || !aligned16(u0)) return WHEAD_ERR_INVALID_ARG;
   const size_t need = kNaAhOff + 2 * (size_t)kMaxB * p.r * 4;
@@ -625,6 +704,8 @@ extern "C" int whead_walk_noalloc(const void* W, const void* E, const whead_para
   WalkArgs a;
   std::memset(&a, 0, sizeof(a));
   a.W = static_cast<const uint16_t*>(W);
+  a.sw = nullptr;
+  a.rw = p.r;
   a.E = static_cast<const uint16_t*>(E);
   a.A = p.A;
   a.c = p.c;

@@ -18,6 +18,7 @@ FLAG_LOGITS_F32 = 1 << 0
 FLAG_FIXED_LATENT = 1 << 1
 FLAG_FORCE_STREAM = 1 << 2
 FLAG_PLACEMENT_CAPS = 1 << 3
+FLAG_W_E4M3 = 1 << 4
 FLAG_FAULT_SKIP_ARRIVAL = 1 << 8
 
 OK = 0
@@ -31,7 +32,7 @@ ERR_INTERNAL = -6
 # Every symbol include/whead.h declares.
 EXPORTS = ("whead_create", "whead_walk", "whead_walk_ex", "whead_walk_host", "whead_status",
            "whead_plan_info", "whead_strerror", "whead_destroy", "whead_walk_noalloc",
-           "whead_set_trace")
+           "whead_set_trace", "whead_quantize_w_e4m3")
 
 
 class WheadParams(ctypes.Structure):
@@ -82,9 +83,10 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     L.whead_strerror.restype = ctypes.c_char_p
     L.whead_destroy.argtypes = [vp]
     L.whead_walk_noalloc.argtypes = [vp, vp, ctypes.POINTER(WheadParams), vp, vp, i32, i32, f32, u64, vp, vp, vp]
+    L.whead_quantize_w_e4m3.argtypes = [vp, i64, i32, vp, vp, vp]
     for name in ("whead_create", "whead_walk", "whead_walk_ex", "whead_walk_host", "whead_status",
                  "whead_plan_info", "whead_destroy", "whead_walk_noalloc",
-           "whead_set_trace"):
+           "whead_set_trace", "whead_quantize_w_e4m3"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L

@@ -49,13 +49,14 @@ def run_gpu(head, dd, B, gamma, T, seed, *, t0=0, base=None, s0=None, want_z=Tru
             "state": None if st is None else st.cpu().numpy()}
 
 
-def check_walk(head, d, dd, *, T=0.0, seed=0, check_state=True, report=None):
-    """Full parity check of one call against the oracle, with the resume rule at near-tie divergences."""
+def check_walk(head, d, dd, *, T=0.0, seed=0, check_state=True, report=None, w_e4m3=None):
+    """Full parity check of one call against the oracle, with the resume rule at near-tie divergences.
+    w_e4m3: (Wq, sw) from the oracle's quantizer when the head runs with E4M3 weights."""
     import torch
     kind = d["kind"]
     B, gamma, V = d["base"].shape
     ref = O.walk(kind, d["W"], d["E"], d["base"], d["s0"], A=d["A"], c=d["c"], T=T, seed=seed,
-                 want_z=True, want_state=True, want_gap=True)
+                 want_z=True, want_state=True, want_gap=True, w_e4m3=w_e4m3)
     scale = float(np.sqrt(np.mean(ref["z"].astype(np.float64) ** 2)))
     near = []
     t_start = 0

@@ -28,6 +28,10 @@ WORKLOADS = {
     "markov_v248064_r256_b1_g16": dict(kind=MARKOV, V=248064, r=256, B=1, gamma=16, T=0.0),
     "markov_v248064_r256_b4_g16": dict(kind=MARKOV, V=248064, r=256, B=4, gamma=16, T=0.0),
     "recurrent_v151936_r256_b1_g15": dict(kind=RECURRENT, V=151936, r=256, B=1, gamma=15, T=0.0),
+    # the same tensors with W in E4M3 (one scale per row) and the state split into two E4M3 vectors
+    "markov_v151936_r256_b1_g16_e4m3": dict(kind=MARKOV, V=151936, r=256, B=1, gamma=16, T=0.0, w="e4m3"),
+    "markov_v248064_r256_b1_g16_e4m3": dict(kind=MARKOV, V=248064, r=256, B=1, gamma=16, T=0.0, w="e4m3"),
+    "markov_v248064_r256_b4_g16_e4m3": dict(kind=MARKOV, V=248064, r=256, B=4, gamma=16, T=0.0, w="e4m3"),
 }
 SWEEP = dict(kind=MARKOV, V=151936, r=256, gammas=(1, 7, 16), Bs=(1, 2, 4, 8, 16), Ts=(0.0, 1.0))
 
