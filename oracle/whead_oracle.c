@@ -34,6 +34,7 @@
  * Build: gcc -O2 -ffp-contract=off -fPIC -shared whead_oracle.c -lm  (no FMA contraction, so that x86
  * and Arm hosts give the same bits).
  */
+#include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
@@ -141,18 +142,21 @@ uint8_t whead_oracle_e4m3_round(float f) {
 }
 
 /*
- * Per-vector E4M3 quantization: scale s = max|x| / 448 (fp32), codes q[k] = E4M3(x[k] / s) (fp32 division).
- * An all-zero vector gets s = 0 and zero codes. Returns s.
+ * Per-vector E4M3 quantization: scale s = max|x| / 448 (fp32 division), its reciprocal inv = 1 / s (fp32
+ * division, once), codes q[k] = E4M3(x[k] * inv) (fp32 product). A vector whose largest magnitude is below
+ * 448 * FLT_MIN (so that inv would not be finite), the all-zero vector included, gets s = 0 and zero codes.
+ * Returns s.
  */
 float whead_oracle_quantize_e4m3(const float* x, int32_t n, uint8_t* q) {
   float amax = 0.0f;
   for (int32_t k = 0; k < n; ++k) amax = fabsf(x[k]) > amax ? fabsf(x[k]) : amax;
-  if (amax == 0.0f) {
+  if (!(amax >= 448.0f * FLT_MIN)) {
     for (int32_t k = 0; k < n; ++k) q[k] = 0;
     return 0.0f;
   }
   const float s = amax / 448.0f;
-  for (int32_t k = 0; k < n; ++k) q[k] = whead_oracle_e4m3_round(x[k] / s);
+  const float inv = 1.0f / s;
+  for (int32_t k = 0; k < n; ++k) q[k] = whead_oracle_e4m3_round(x[k] * inv);
   return s;
 }
 

@@ -109,7 +109,7 @@ __host__ __device__ constexpr uint32_t wl_entry(int j, uint32_t tier, int col) {
 
 // Shared-memory layout after the W tier (byte offsets from the 1024-aligned base).
 struct SmemLayout {
-  int red, win, misc, base, h, a, sw, total;
+  int red, win, misc, base, h, a, sw, q, qs, total;
   __host__ __device__ static SmemLayout make(int smem_w_bytes, int B, int r, int ra, bool recurrent, int ng,
                                              bool f8 = false) {
     SmemLayout L;
@@ -120,7 +120,9 @@ struct SmemLayout {
     L.h = L.base + B * ng * kGroupRows * 4;     // recurrent: [B][r] fp32
     L.a = L.h + (recurrent ? B * r * 4 : 0);    // recurrent: [ra][r] fp32
     L.sw = L.a + (recurrent ? ra * r * 4 : 0);  // E4M3 weights: [ng * 16] fp32 row scales
-    L.total = L.sw + (f8 ? ng * kGroupRows * 4 : 0);
+    L.q = L.sw + (f8 ? ng * kGroupRows * 4 : 0);  // E4M3: [2B][r + 16] codes of each walk's hi and lo vectors
+    L.qs = L.q + (f8 ? 2 * B * (r + 16) : 0);     // E4M3: [2B] fp32 scales of those vectors
+    L.total = L.qs + (f8 ? 2 * kMaxB * 4 : 0);
     return L;
   }
 };
@@ -383,7 +385,8 @@ __device__ __forceinline__ float warp_absmax(float m) {
 }
 
 // Quantizes a vector spread over the warp (lane L holds elements [L * EPL, L * EPL + EPL)): scale
-// s = max|x| / 448, codes E4M3(x / s) packed four to a word, or s = 0 and zero codes for an all-zero vector.
+// s = max|x| / 448, inv = 1 / s (both correctly rounded), codes E4M3(x * inv) packed four to a word. A vector
+// whose largest magnitude is below 448 * FLT_MIN (inv would not be finite) gets s = 0 and zero codes.
 template <int EPL>
 __device__ __forceinline__ float quantize_e4m3_warp(const float (&x)[EPL], uint32_t (&q)[EPL / 4]) {
   const float amax = [&] {
@@ -392,34 +395,25 @@ __device__ __forceinline__ float quantize_e4m3_warp(const float (&x)[EPL], uint3
     for (int e = 0; e < EPL; ++e) m = fmaxf(m, fabsf(x[e]));
     return warp_absmax(m);
   }();
-  const float s = amax == 0.f ? 0.f : __fdiv_rn(amax, 448.f);
+  const bool zero = !(amax >= 448.f * 1.17549435e-38f);
+  const float s = zero ? 0.f : __fdiv_rn(amax, 448.f);
+  const float inv = zero ? 0.f : __frcp_rn(s);
 #pragma unroll
   for (int w = 0; w < EPL / 4; ++w)
-    q[w] = s == 0.f ? 0u
-                    : e4m3x4(__fdiv_rn(x[4 * w], s), __fdiv_rn(x[4 * w + 1], s), __fdiv_rn(x[4 * w + 2], s),
-                             __fdiv_rn(x[4 * w + 3], s));
+    q[w] = zero ? 0u
+                : e4m3x4(__fmul_rn(x[4 * w], inv), __fmul_rn(x[4 * w + 1], inv), __fmul_rn(x[4 * w + 2], inv),
+                         __fmul_rn(x[4 * w + 3], inv));
   return s;
 }
 
-// B fragments of the E4M3 projection for B <= 4 walks: column 2w holds walk w's hi vector, column 2w + 1 its
-// lo vector (the residual). load(w, x) puts walk w's state elements [lane * EPL, lane * EPL + EPL) in x. The
-// fragment word i of box bx of lane (g, c) is state bytes 128 bx + 32 c + 4 i (the same order as the bf16
-// path's), gathered by shuffles from the lane that quantized them. s1c / s2c: the scales of walk c (the
-// walk whose sums this lane's accumulator columns 2c, 2c + 1 hold). Every lane of the warp must call this.
+// Warp routine: splits each walk's state into two E4M3 vectors (hi, and the residual lo) and stores them in
+// shared memory: row 2w (hi) and 2w + 1 (lo) of s_q (rows of r + 16 bytes, so that the rows a warp reads at
+// once start on different banks), scales s_qs[2w], s_qs[2w + 1]. load(w, x) puts walk w's state elements
+// [lane * EPL, lane * EPL + EPL) in x. Every lane of the warp must call this.
 template <int KB, typename Load>
-__device__ __forceinline__ void bfrag_e4m3(uint32_t (&bf)[1][KB][8], float& s1c, float& s2c, int B, int lane,
-                                           Load load) {
+__device__ __forceinline__ void split_state_smem(uint8_t* s_q, float* s_qs, int B, int r, int lane, Load load) {
   constexpr int EPL = 4 * KB;  // r = 128 KB elements over 32 lanes
-  const int g = lane >> 2, c = lane & 3;
-#pragma unroll
-  for (int bx = 0; bx < KB; ++bx)
-#pragma unroll
-    for (int i = 0; i < 8; ++i) bf[0][bx][i] = 0u;
-  s1c = 0.f;
-  s2c = 0.f;
-#pragma unroll
-  for (int w = 0; w < 4; ++w) {
-    if (w >= B) break;
+  for (int w = 0; w < B; ++w) {
     float x[EPL];
     load(w, x);
     uint32_t qh[KB], ql[KB];
@@ -431,23 +425,45 @@ __device__ __forceinline__ void bfrag_e4m3(uint32_t (&bf)[1][KB][8], float& s1c,
       res[e] = __fsub_rn(x[e], __fmul_rn(s1, e4m3_value(code)));
     }
     const float s2 = quantize_e4m3_warp<EPL>(res, ql);
+    uint32_t* dh = reinterpret_cast<uint32_t*>(s_q + (2 * w) * (r + 16) + lane * EPL);
+    uint32_t* dl = reinterpret_cast<uint32_t*>(s_q + (2 * w + 1) * (r + 16) + lane * EPL);
 #pragma unroll
-    for (int bx = 0; bx < KB; ++bx)
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const int o = 128 * bx + 32 * c + 4 * i;  // state byte (= element) offset of this fragment word
-        // 128 bx and 32 c are multiples of EPL (4 or 8), so the word within the source lane depends on i only
-        const int src = o / EPL, wi = ((4 * i) % EPL) / 4;
-        const uint32_t h = __shfl_sync(0xffffffffu, qh[wi], src);
-        const uint32_t l = __shfl_sync(0xffffffffu, ql[wi], src);
-        if ((g >> 1) == w) bf[0][bx][i] = (g & 1) ? l : h;
-      }
-    if (c == w) {
-      s1c = s1;
-      s2c = s2;
+    for (int k = 0; k < KB; ++k) {
+      dh[k] = qh[k];
+      dl[k] = ql[k];
+    }
+    if (lane == 0) {
+      s_qs[2 * w] = s1;
+      s_qs[2 * w + 1] = s2;
     }
   }
 }
+
+// B fragments of the E4M3 projection for B <= 4 walks, from the split state in shared memory: column 2w holds
+// walk w's hi vector, column 2w + 1 its lo vector, so lane (g, c) reads row g; fragment word i of box bx is
+// bytes 128 bx + 32 c + 4 i of that row (the bf16 path's order). s1c / s2c: the scales of walk c, whose sums
+// this lane's accumulator columns 2c and 2c + 1 hold.
+template <int KB>
+__device__ __forceinline__ void bfrag_from_split_smem(uint32_t (&bf)[1][KB][8], float& s1c, float& s2c,
+                                                      const uint8_t* s_q, const float* s_qs, int B, int r, int lane) {
+  const int g = lane >> 2, c = lane & 3;
+  const bool live = (g >> 1) < B;
+  const uint8_t* row = s_q + g * (r + 16);
+#pragma unroll
+  for (int bx = 0; bx < KB; ++bx) {
+    uint4 x0 = make_uint4(0u, 0u, 0u, 0u), x1 = x0;
+    if (live) {
+      const uint4* p = reinterpret_cast<const uint4*>(row + 128 * bx + 32 * c);
+      x0 = p[0];
+      x1 = p[1];
+    }
+    bf[0][bx][0] = x0.x; bf[0][bx][1] = x0.y; bf[0][bx][2] = x0.z; bf[0][bx][3] = x0.w;
+    bf[0][bx][4] = x1.x; bf[0][bx][5] = x1.y; bf[0][bx][6] = x1.z; bf[0][bx][7] = x1.w;
+  }
+  s1c = c < B ? s_qs[2 * c] : 0.f;
+  s2c = c < B ? s_qs[2 * c + 1] : 0.f;
+}
+
 
 // Rows g / g + 8 of a box as loaded ([R0 | S0 | R1 | S1]: chunk 2c then 2c + 1 of each row) to fragment
 // order: op m = 2 rho + h takes {R_rho[2h], S_rho[2h], R_rho[2h + 1], S_rho[2h + 1]}.
@@ -579,6 +595,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* s_h = reinterpret_cast<float*>(smem + L.h);
   float* s_A = reinterpret_cast<float*>(smem + L.a);
   float* s_sw = reinterpret_cast<float*>(smem + L.sw);  // E4M3 weights: scales of this CTA's rows
+  uint8_t* s_q = smem + L.q;                            // E4M3 weights: each walk's state as two E4M3 vectors
+  float* s_qs = reinterpret_cast<float*>(smem + L.qs);  // and their scales
   static_assert(!F8 || NH == 1, "E4M3 weights take two accumulator columns per walk: at most 4 walks");
 
   const uint32_t mbar = smem_u32(s_mbar);
@@ -716,6 +734,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       out[96] = make_uint4(r1.z, s1.z, r1.w, s1.w);
     }
   }
+  // E4M3 weights: warp 0 splits the initial states into two E4M3 vectors each (read by every warp after
+  // the barrier)
+  if constexpr (F8) {
+    if (warp == 0)
+      split_state_smem<KB>(s_q, s_qs, B, r, lane, [&](int w, auto& x) {
+        const float* src = P.s0 + (int64_t)w * r + lane * 4 * KB;
+#pragma unroll
+        for (int e = 0; e < 4 * KB; ++e) x[e] = src[e];
+      });
+  }
   tmem_fence_before();
   __syncthreads();
   tmem_fence_after();
@@ -754,14 +782,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t bf[NH][KB][8];
     // E4M3 weights: the scales of walk c's two state vectors (this lane's accumulator columns 2c, 2c + 1)
     float es1 = 0.f, es2 = 0.f;
-    // the state of walk w as fp32 (initial state, or the recurrent state in shared memory)
-    auto load_f32_state = [&](int w, auto& x) {
-      const float* src = (recurrent ? s_h : P.s0) + (int64_t)w * r + lane * 4 * KB;
-#pragma unroll
-      for (int e = 0; e < 4 * KB; ++e) x[e] = src[e];
-    };
     if constexpr (F8) {
-      bfrag_e4m3<KB>(bf, es1, es2, B, lane, load_f32_state);
+      bfrag_from_split_smem<KB>(bf, es1, es2, s_q, s_qs, B, r, lane);
     } else {
 #pragma unroll
       for (int h = 0; h < NH; ++h) {
@@ -1116,6 +1138,34 @@ __global__ void __launch_bounds__(kThreads, 1)
           atomicCAS(P.status, 0, kStatusTimeout);
           *s_abort = 1;
         }
+        // E4M3 weights, Markov: the winners' E rows, split into two E4M3 vectors each, for every warp's next
+        // B fragments (a winner outside W is skipped here; the check after the barrier ends the walk)
+        if constexpr (F8) {
+          if (!late && !recurrent && !(P.flags & kFlagFixedLatent)) {
+            __syncwarp();
+            split_state_smem<KB>(s_q, s_qs, B, r, lane, [&](int w, auto& x) {
+              const int32_t xw = s_win[w];
+              uint32_t u[2 * KB];
+#pragma unroll
+              for (int e = 0; e < 2 * KB; ++e) u[e] = 0u;
+              if (xw >= 0 && (int64_t)xw < V) {
+                const uint16_t* er = P.E + (int64_t)xw * r + lane * 4 * KB;
+                if constexpr (KB == 2) {
+                  const uint4 v = __ldg(reinterpret_cast<const uint4*>(er));
+                  u[0] = v.x; u[1] = v.y; u[2] = v.z; u[3] = v.w;
+                } else {
+                  const uint2 v = __ldg(reinterpret_cast<const uint2*>(er));
+                  u[0] = v.x; u[1] = v.y;
+                }
+              }
+#pragma unroll
+              for (int e = 0; e < 2 * KB; ++e) {
+                x[2 * e] = __uint_as_float(u[e] << 16);
+                x[2 * e + 1] = __uint_as_float(u[e] & 0xFFFF0000u);
+              }
+            });
+          }
+        }
         trace_stamp(P, 2 + kTraceStampsPerStep * t + 2);
       }
       __syncthreads();
@@ -1133,23 +1183,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (P.flags & kFlagFixedLatent) continue;
       if (!recurrent) {
         if constexpr (F8) {
-          // the winners' E rows, split into two E4M3 vectors by every warp
-          bfrag_e4m3<KB>(bf, es1, es2, B, lane, [&](int w, auto& x) {
-            const uint16_t* er = P.E + (int64_t)s_win[w] * r + lane * 4 * KB;
-            uint32_t u[2 * KB];
-            if constexpr (KB == 2) {
-              const uint4 v = __ldg(reinterpret_cast<const uint4*>(er));
-              u[0] = v.x; u[1] = v.y; u[2] = v.z; u[3] = v.w;
-            } else {
-              const uint2 v = __ldg(reinterpret_cast<const uint2*>(er));
-              u[0] = v.x; u[1] = v.y;
-            }
-#pragma unroll
-            for (int e = 0; e < 2 * KB; ++e) {
-              x[2 * e] = __uint_as_float(u[e] << 16);
-              x[2 * e + 1] = __uint_as_float(u[e] & 0xFFFF0000u);
-            }
-          });
+          // the winners' E rows were split into shared memory by the exchange warp
+          bfrag_from_split_smem<KB>(bf, es1, es2, s_q, s_qs, B, r, lane);
         } else {
 #pragma unroll
           for (int h = 0; h < NH; ++h) {
@@ -1175,7 +1210,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncthreads();
         if constexpr (F8) {
-          bfrag_e4m3<KB>(bf, es1, es2, B, lane, load_f32_state);
+          if (warp == 0)
+            split_state_smem<KB>(s_q, s_qs, B, r, lane, [&](int w, auto& x) {
+              const float* src = s_h + w * r + lane * 4 * KB;
+#pragma unroll
+              for (int e = 0; e < 4 * KB; ++e) x[e] = src[e];
+            });
+          __syncthreads();
+          bfrag_from_split_smem<KB>(bf, es1, es2, s_q, s_qs, B, r, lane);
         } else {
 #pragma unroll
           for (int h = 0; h < NH; ++h) {

@@ -165,3 +165,13 @@ def test_e4m3_walk_resume_from_any_step(kind, T):
                       c=d["c"], T=T, seed=11, t0=t0, want_z=True, want_state=True, w_e4m3=(Wq, sw))
         np.testing.assert_array_equal(part["tokens"], full["tokens"][:, t0:])
         np.testing.assert_array_equal(part["z"], full["z"][:, t0:])
+
+
+def test_vectors_below_the_normal_range_quantize_to_zero():
+    """448 * FLT_MIN is the smallest largest-magnitude with a finite reciprocal scale; below it the vector is
+    taken as zero (scale 0, zero codes), at it the scale is exactly FLT_MIN."""
+    tiny = np.float32(448.0) * np.float32(np.finfo(np.float32).tiny)
+    s, q = O.quantize_e4m3(np.array([tiny * np.float32(0.5), -tiny * np.float32(0.25)], dtype=np.float32))
+    assert s == 0.0 and not q.any()
+    s, q = O.quantize_e4m3(np.array([tiny, 0.0], dtype=np.float32))
+    assert s == np.finfo(np.float32).tiny and q[0] == 0x7E
