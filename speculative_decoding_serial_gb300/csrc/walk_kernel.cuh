@@ -168,6 +168,28 @@ __device__ __forceinline__ void mma_bf16_16816_z(float (&d)[4], uint32_t a0, uin
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
 }
 
+// f16 x f16 -> fp32, 16 x 8 x 16 (used for E4M3 data, which f16 holds exactly).
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                              uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_f16_16816_z(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                                uint32_t b0, uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%10,%10,%10,%10};"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(0.0f));
+}
+
+// Four E4M3 codes (one word) to two f16x2 words: .x from bytes 0 and 1, .y from bytes 2 and 3 (exact).
+__device__ __forceinline__ uint2 e4m3x4_to_f16(uint32_t w) {
+  uint32_t lo, hi;
+  asm("{\n .reg .b16 l, h;\n mov.b32 {l, h}, %2;\n cvt.rn.f16x2.e4m3x2 %0, l;\n cvt.rn.f16x2.e4m3x2 %1, h;\n}\n"
+      : "=r"(lo), "=r"(hi) : "r"(w));
+  return make_uint2(lo, hi);
+}
+
 // E4M3 x E4M3 -> fp32, 16 x 8 x 32. Its fragments have the bf16 16 x 8 x 16 layout byte for byte (each 32-bit
 // register holds four 8-bit values where the bf16 layout holds two 16-bit ones), so the same storage orders
 // serve both formats.
@@ -337,20 +359,28 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // The four ops of a box go to four independent accumulators so that they issue back to back. The box's
 // A operands are stored in fragment order: a[4m .. 4m + 3] = {a0, a1, a2, a3} of op m (m = 2 rho + h), so
 // each op reads four consecutive registers as they were loaded.
+// B fragment words per box: 8 (bf16, or E4M3 codes four to a word), 16 when E4M3 codes are held as f16 pairs.
+template <bool F8> constexpr int kBfWords = F8 ? 16 : 8;
+
 template <int KB, int NH, bool F8 = false>
 __device__ __forceinline__ void mma_box(float (&acc)[4][NH][4], const uint32_t (&a)[16],
-                                        const uint32_t (&bf)[NH][KB][8], int bx) {
+                                        const uint32_t (&bf)[NH][KB][kBfWords<F8>], int bx) {
 #pragma unroll
   for (int m = 0; m < 4; ++m) {
 #pragma unroll
     for (int n = 0; n < NH; ++n) {
       if constexpr (F8) {
+        // One 16 x 8 x 32 step on E4M3 codes as two f16 16 x 8 x 16 steps: the first takes the low and the
+        // high code pairs of the A words that hold k = 4c .. 4c + 3 (rows g, g + 8) against the same pairs of
+        // the B word for those k; the second does the same for k = 16 + 4c .. 16 + 4c + 3. A and B split
+        // every 4-value word the same way, so each product meets its partner.
+        const uint2 p0 = e4m3x4_to_f16(a[4 * m]), p1 = e4m3x4_to_f16(a[4 * m + 1]);
+        const uint2 p2 = e4m3x4_to_f16(a[4 * m + 2]), p3 = e4m3x4_to_f16(a[4 * m + 3]);
         if (bx == 0)
-          mma_e4m3_16832_z(acc[m][n], a[4 * m], a[4 * m + 1], a[4 * m + 2], a[4 * m + 3], bf[n][bx][2 * m],
-                           bf[n][bx][2 * m + 1]);
+          mma_f16_16816_z(acc[m][n], p0.x, p1.x, p0.y, p1.y, bf[n][bx][4 * m], bf[n][bx][4 * m + 1]);
         else
-          mma_e4m3_16832(acc[m][n], a[4 * m], a[4 * m + 1], a[4 * m + 2], a[4 * m + 3], bf[n][bx][2 * m],
-                         bf[n][bx][2 * m + 1]);
+          mma_f16_16816(acc[m][n], p0.x, p1.x, p0.y, p1.y, bf[n][bx][4 * m], bf[n][bx][4 * m + 1]);
+        mma_f16_16816(acc[m][n], p2.x, p3.x, p2.y, p3.y, bf[n][bx][4 * m + 2], bf[n][bx][4 * m + 3]);
       } else {
         if (bx == 0)
           mma_bf16_16816_z(acc[m][n], a[4 * m], a[4 * m + 1], a[4 * m + 2], a[4 * m + 3], bf[n][bx][2 * m],
@@ -444,7 +474,7 @@ __device__ __forceinline__ void split_state_smem(uint8_t* s_q, float* s_qs, int 
 // bytes 128 bx + 32 c + 4 i of that row (the bf16 path's order). s1c / s2c: the scales of walk c, whose sums
 // this lane's accumulator columns 2c and 2c + 1 hold.
 template <int KB>
-__device__ __forceinline__ void bfrag_from_split_smem(uint32_t (&bf)[1][KB][8], float& s1c, float& s2c,
+__device__ __forceinline__ void bfrag_from_split_smem(uint32_t (&bf)[1][KB][16], float& s1c, float& s2c,
                                                       const uint8_t* s_q, const float* s_qs, int B, int r, int lane) {
   const int g = lane >> 2, c = lane & 3;
   const bool live = (g >> 1) < B;
@@ -457,8 +487,14 @@ __device__ __forceinline__ void bfrag_from_split_smem(uint32_t (&bf)[1][KB][8], 
       x0 = p[0];
       x1 = p[1];
     }
-    bf[0][bx][0] = x0.x; bf[0][bx][1] = x0.y; bf[0][bx][2] = x0.z; bf[0][bx][3] = x0.w;
-    bf[0][bx][4] = x1.x; bf[0][bx][5] = x1.y; bf[0][bx][6] = x1.z; bf[0][bx][7] = x1.w;
+    // code word i becomes f16 words 2i (its codes 0, 1) and 2i + 1 (codes 2, 3)
+    const uint32_t w[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint2 h = e4m3x4_to_f16(w[i]);
+      bf[0][bx][2 * i] = h.x;
+      bf[0][bx][2 * i + 1] = h.y;
+    }
   }
   s1c = c < B ? s_qs[2 * c] : 0.f;
   s2c = c < B ? s_qs[2 * c + 1] : 0.f;
@@ -779,7 +815,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
 
-    uint32_t bf[NH][KB][8];
+    uint32_t bf[NH][KB][kBfWords<F8>];
     // E4M3 weights: the scales of walk c's two state vectors (this lane's accumulator columns 2c, 2c + 1)
     float es1 = 0.f, es2 = 0.f;
     if constexpr (F8) {
