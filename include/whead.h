@@ -79,6 +79,11 @@ typedef struct {
   int32_t cap_smem;    /* with WHEAD_FLAG_PLACEMENT_CAPS: most groups per CTA in shared memory (>= 0) */
   int32_t cap_tmem;    /* with WHEAD_FLAG_PLACEMENT_CAPS: most groups per CTA in tensor memory (>= 0) */
   int32_t cap_rf;      /* with WHEAD_FLAG_PLACEMENT_CAPS: most groups per CTA in registers (>= 0) */
+  int64_t v_offset;    /* vocabulary sharding: global index of W's first row (a multiple of 16; 0 for a whole
+                          vocabulary). Rows of W are rows v_offset .. v_offset + V - 1 of the vocabulary:
+                          tokens, packed keys and the noise counters use global rows, and E must hold the
+                          global rows (E is indexed by the winner). */
+  int64_t e_rows;      /* rows of E (0 = v_offset + V); winners handed to whead_advance must be below it */
 } whead_params;
 
 /* Placement chosen for a batch size (whead_plan_info). Groups are 16 consecutive rows of W. */
@@ -124,6 +129,27 @@ int whead_walk(whead_t* h, const float* base, const float* u0, int32_t B, int32_
  */
 int whead_walk_ex(whead_t* h, const float* base, const float* s0, int32_t B, int32_t gamma, float T,
                   uint64_t seed, int64_t t0, int32_t* out_tokens, void* out_logits, float* out_state);
+
+/*
+ * whead_walk_ex that also returns each step's winning packed key (out_keys: NULL, or B x gamma uint64,
+ * device, 8-byte aligned): ord(key) << 32 | (2^32 - 1 - row), where key is the winner's selection key (z, or
+ * z / T + Gumbel noise), ord maps fp32 to uint32 in order (negative values ~bits, others bits | 2^31, -0 as +0)
+ * and row is the global row. The largest key over shards is the winner over the union of their rows, ties
+ * going to the lowest row (Fig. 8's packed selection, taken across GPUs for a sharded vocabulary).
+ */
+int whead_walk_keys(whead_t* h, const float* base, const float* s0, int32_t B, int32_t gamma, float T,
+                    uint64_t seed, int64_t t0, int32_t* out_tokens, uint64_t* out_keys, void* out_logits,
+                    float* out_state);
+
+/*
+ * The state after one step for given winners (abstract: the state advance, done on the GPU): x (B int32,
+ * global rows of E, device), s (B x r fp32, the state that step projected, device) -> s_next (B x r fp32,
+ * device). Markov: s_next = E[x]; recurrent: tanh(A s + E[x] + c), in the walk kernel's order of operations.
+ * Enqueued on the handle's stream. A winner outside E gives a zero state and the device status
+ * WHEAD_ERR_INTERNAL (see whead_status). For a vocabulary sharded over GPUs, every rank advances with the
+ * winner of the merged keys.
+ */
+int whead_advance(whead_t* h, const int32_t* x, const float* s, float* s_next, int32_t B);
 
 /*
  * Synchronous walk on HOST buffers (same arguments as whead_walk, all pointers host memory; pinned

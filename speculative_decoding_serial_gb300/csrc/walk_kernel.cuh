@@ -66,6 +66,7 @@ struct WalkArgs {
   const float* base;
   const float* s0;
   int32_t* tokens;
+  unsigned long long* keys;  // optional: each step's winning packed key per walk, ord(key) << 32 | ~row
   void* logits;
   float* state;
   unsigned long long* slots;        // [2 step parities][grid][B] tagged keys for this call
@@ -78,6 +79,7 @@ struct WalkArgs {
   unsigned long long* trace;  // optional phase stamps: [grid][trace_stride] (clock64 half, globaltimer half)
   int32_t trace_stride;
   int64_t V;
+  int64_t v_offset;  // global index of W's first row (a vocabulary shard); a multiple of 16
   int64_t t0;
   uint64_t seed;
   uint64_t timeout_ns;
@@ -638,6 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t mbar = smem_u32(s_mbar);
   trace_stamp(P, 0);
   const int64_t row_base = (int64_t)cta * P.ng * kGroupRows;
+  const int64_t vg_base = P.v_offset + row_base;  // global row of the CTA's first row (keys, noise, tokens)
   const int rows_cta = P.ng * kGroupRows;
   const int my_count = P.wl_count[warp];
   const uint32_t my_entry = (lane < my_count) ? P.wl[warp][lane] : 0u;
@@ -999,21 +1002,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           // greedy without logits: keys only (a loop of its own, so it carries no sampling code)
 #pragma unroll 4
           for (int lr = tid; lr < valid; lr += kThreads)
-            bestk = umax64(bestk, pack_key(s_base[lr], (uint32_t)(row_base + lr)));
+            bestk = umax64(bestk, pack_key(s_base[lr], (uint32_t)(vg_base + lr)));
         } else if (!sampled) {
           for (int lr = tid; lr < valid; lr += kThreads) {
             const float z = s_base[lr];
             if (want_f32) reinterpret_cast<float*>(P.logits)[obase + lr] = z;
             else reinterpret_cast<__nv_bfloat16*>(P.logits)[obase + lr] = __float2bfloat16_rn(z);
-            bestk = umax64(bestk, pack_key(z, (uint32_t)(row_base + lr)));
+            bestk = umax64(bestk, pack_key(z, (uint32_t)(vg_base + lr)));
           }
         } else {
           // sampled: each thread scores four consecutive rows with one Philox call (the CTA's first row is a
-          // multiple of 16, so row_base + lr is a multiple of 4)
+          // multiple of 16, and so is the shard's first row: vg_base + lr is a multiple of 4)
           for (int lr = 4 * tid; lr < valid; lr += 4 * kThreads) {
             const float4 z4 = *reinterpret_cast<const float4*>(s_base + lr);
             const float zz[4] = {z4.x, z4.y, z4.z, z4.w};
-            const uint32_t v0 = (uint32_t)(row_base + lr);
+            const uint32_t v0 = (uint32_t)(vg_base + lr);
             const uint4 o = philox_quad(P.seed, 0u, tau, v0 >> 2);
             const uint32_t ww[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
@@ -1043,20 +1046,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!sampled && !P.logits) {
 #pragma unroll 4
             for (int lr = tid / Bp; lr < valid; lr += stride)
-              bestk = umax64(bestk, pack_key(zrow[lr], (uint32_t)(row_base + lr)));
+              bestk = umax64(bestk, pack_key(zrow[lr], (uint32_t)(vg_base + lr)));
           } else if (!sampled) {
             for (int lr = tid / Bp; lr < valid; lr += stride) {
               const float z = zrow[lr];
               if (want_f32) reinterpret_cast<float*>(P.logits)[obase + lr] = z;
               else reinterpret_cast<__nv_bfloat16*>(P.logits)[obase + lr] = __float2bfloat16_rn(z);
-              bestk = umax64(bestk, pack_key(z, (uint32_t)(row_base + lr)));
+              bestk = umax64(bestk, pack_key(z, (uint32_t)(vg_base + lr)));
             }
           } else {
             // sampled: four consecutive rows per Philox call, as for a single walk
             for (int lr = 4 * (tid / Bp); lr < valid; lr += 4 * stride) {
               const float4 z4 = *reinterpret_cast<const float4*>(zrow + lr);
               const float zz[4] = {z4.x, z4.y, z4.z, z4.w};
-              const uint32_t v0 = (uint32_t)(row_base + lr);
+              const uint32_t v0 = (uint32_t)(vg_base + lr);
               const uint4 o = philox_quad(P.seed, (uint32_t)n, tau, v0 >> 2);
               const uint32_t ww[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
@@ -1166,7 +1169,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane == 0) {
             const int32_t x = (int32_t)(0xFFFFFFu - ((uint32_t)wk & 0xFFFFFFu));
             s_win[n] = x;
-            if (cta == 0) P.tokens[(int64_t)n * gamma + t] = x;
+            if (cta == 0) {
+              P.tokens[(int64_t)n * gamma + t] = x;
+              if (P.keys) P.keys[(int64_t)n * gamma + t] = ((wk >> 24) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)x);
+            }
           }
         }
         late = __any_sync(0xffffffffu, late);
@@ -1184,7 +1190,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               uint32_t u[2 * KB];
 #pragma unroll
               for (int e = 0; e < 2 * KB; ++e) u[e] = 0u;
-              if (xw >= 0 && (int64_t)xw < V) {
+              if ((int64_t)xw >= P.v_offset && (int64_t)xw < P.v_offset + V) {
                 const uint16_t* er = P.E + (int64_t)xw * r + lane * 4 * KB;
                 if constexpr (KB == 2) {
                   const uint4 v = __ldg(reinterpret_cast<const uint4*>(er));
@@ -1209,7 +1215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // winners must be rows of W (a failed exchange would show up here)
       bool bad = false;
-      for (int n = 0; n < B; ++n) bad |= (s_win[n] < 0 || (int64_t)s_win[n] >= V);
+      for (int n = 0; n < B; ++n) bad |= ((int64_t)s_win[n] < P.v_offset || (int64_t)s_win[n] >= P.v_offset + V);
       if (bad) {
         if (tid == 0) atomicCAS(P.status, 0, kStatusInternal);
         break;

@@ -254,6 +254,40 @@ int launch(whead_t* h, const Plan& pl, const WalkArgs& a, int NH) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The next state of B walks for given winners x (global rows of E), one warp per (walk, element): Markov
+// s_next[b] = E[x_b] (bf16 to fp32); recurrent s_next[b][i] = tanh(A[i,:] . s[b] + E[x_b, i] + c[i]) with the
+// walk kernel's own order of operations (lane-strided fmaf, then a butterfly sum). A winner outside E gives a
+// zero state and the status word WHEAD_ERR_INTERNAL.
+__global__ void advance_kernel(int kind, const uint16_t* __restrict__ E, const float* __restrict__ A,
+                               const float* __restrict__ c, const int32_t* __restrict__ x, const float* __restrict__ s,
+                               float* __restrict__ s_next, int B, int r, int64_t e_rows, int* status) {
+  const int wi = (int)(blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32), lane = threadIdx.x & 31;
+  if (wi >= B * r) return;  // the same for every lane of the warp
+  const int b = wi / r, i = wi % r;
+  const int64_t xb = x[b];
+  if (xb < 0 || xb >= e_rows) {
+    if (lane == 0) {
+      s_next[(int64_t)b * r + i] = 0.f;
+      atomicCAS(status, 0, kStatusInternal);
+    }
+    return;
+  }
+  const float e = __uint_as_float((uint32_t)E[xb * r + i] << 16);
+  if (kind == WHEAD_MARKOV) {
+    if (lane == 0) s_next[(int64_t)b * r + i] = e;
+    return;
+  }
+  float acc = 0.f;
+  for (int k = lane; k < r; k += 32) acc = fmaf(A[(int64_t)i * r + k], s[(int64_t)b * r + k], acc);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+  if (lane == 0) {
+    float pre = __fadd_rn(acc, e);
+    if (c) pre = __fadd_rn(pre, c[i]);
+    s_next[(int64_t)b * r + i] = tanhf(pre);
+  }
+}
+
 // E4M3 weights: one warp per row quantizes it as a vector (scale max|w| / 448, codes E4M3(w / s)) with the
 // same warp routine the walk uses for its state. EPL = r / 32 elements per lane.
 template <int EPL>
@@ -344,6 +378,9 @@ int whead_create(const void* W, const void* E, const whead_params* params, whead
   if (!aligned16(W) || !aligned16(E)) return WHEAD_ERR_INVALID_ARG;
   const bool f8 = (p.flags & WHEAD_FLAG_W_E4M3) != 0u;
   if (f8 && ((p.r != 128 && p.r != 256) || p.max_B > 4)) return WHEAD_ERR_UNSUPPORTED;
+  if (p.v_offset < 0 || (p.v_offset & 15) || p.e_rows < 0) return WHEAD_ERR_INVALID_ARG;
+  if (p.v_offset + p.V >= (int64_t)1 << 24 || p.e_rows >= (int64_t)1 << 24) return WHEAD_ERR_UNSUPPORTED;
+  if (p.e_rows > 0 && p.e_rows < p.v_offset + p.V) return WHEAD_ERR_INVALID_ARG;
 
   whead_t* h = new (std::nothrow) whead_s();
   if (!h) return WHEAD_ERR_INVALID_ARG;
@@ -423,9 +460,10 @@ int whead_create(const void* W, const void* E, const whead_params* params, whead
   return WHEAD_OK;
 }
 
-int whead_walk_ex(whead_t* h, const float* base, const float* s0, int32_t B, int32_t gamma, float T, uint64_t seed,
-                  int64_t t0, int32_t* out_tokens, void* out_logits, float* out_state) {
+int whead_walk_keys(whead_t* h, const float* base, const float* s0, int32_t B, int32_t gamma, float T, uint64_t seed,
+                    int64_t t0, int32_t* out_tokens, uint64_t* out_keys, void* out_logits, float* out_state) {
   if (!h || !base || !s0 || !out_tokens) return WHEAD_ERR_INVALID_ARG;
+  if (out_keys && (reinterpret_cast<uintptr_t>(out_keys) & 7u)) return WHEAD_ERR_INVALID_ARG;
   if (B < 1 || B > h->p.max_B || gamma < 1 || gamma > h->p.max_gamma || t0 < 0) return WHEAD_ERR_INVALID_ARG;
   if (!(T >= 0.0f) || T != T || T > 3.0e38f) return WHEAD_ERR_INVALID_ARG;
   if (!aligned16(s0) || (out_state && !aligned16(out_state))) return WHEAD_ERR_INVALID_ARG;
@@ -444,6 +482,7 @@ int whead_walk_ex(whead_t* h, const float* base, const float* s0, int32_t B, int
   a.base = base;
   a.s0 = s0;
   a.tokens = out_tokens;
+  a.keys = reinterpret_cast<unsigned long long*>(out_keys);
   a.logits = out_logits;
   a.state = out_state;
   const uint32_t par = h->parity & 1u;
@@ -459,6 +498,7 @@ int whead_walk_ex(whead_t* h, const float* base, const float* s0, int32_t B, int
     a.trace_stride = trace_stride_for(gamma);
   }
   a.V = h->p.V;
+  a.v_offset = h->p.v_offset;
   a.t0 = t0;
   a.seed = seed;
   a.timeout_ns = (uint64_t)h->p.timeout_us * 1000ull;
@@ -484,9 +524,24 @@ int whead_walk_ex(whead_t* h, const float* base, const float* s0, int32_t B, int
   return rc;
 }
 
+int whead_walk_ex(whead_t* h, const float* base, const float* s0, int32_t B, int32_t gamma, float T, uint64_t seed,
+                  int64_t t0, int32_t* out_tokens, void* out_logits, float* out_state) {
+  return whead_walk_keys(h, base, s0, B, gamma, T, seed, t0, out_tokens, nullptr, out_logits, out_state);
+}
+
 int whead_walk(whead_t* h, const float* base, const float* u0, int32_t B, int32_t gamma, float T, uint64_t seed,
                int32_t* out_tokens, void* out_logits) {
   return whead_walk_ex(h, base, u0, B, gamma, T, seed, 0, out_tokens, out_logits, nullptr);
+}
+
+int whead_advance(whead_t* h, const int32_t* x, const float* s, float* s_next, int32_t B) {
+  if (!h || !x || !s || !s_next) return WHEAD_ERR_INVALID_ARG;
+  if (B < 1 || B > h->p.max_B) return WHEAD_ERR_INVALID_ARG;
+  const int64_t e_rows = h->p.e_rows > 0 ? h->p.e_rows : h->p.v_offset + h->p.V;
+  const int warps = B * h->p.r;
+  advance_kernel<<<(warps + 7) / 8, 256, 0, h->stream>>>(h->p.kind, h->E, h->p.A, h->p.c, x, s, s_next, B, h->p.r,
+                                                       e_rows, h->s.status);
+  return cudaGetLastError() == cudaSuccess ? WHEAD_OK : WHEAD_ERR_CUDA;
 }
 
 int whead_walk_host(whead_t* h, const float* base_host, const float* u0_host, int32_t B, int32_t gamma, float T,
@@ -674,6 +729,8 @@ extern "C" int whead_walk_noalloc(const void* W, const void* E, const whead_para
   if (p.r != 64 && p.r != 128 && p.r != 192 && p.r != 256) return WHEAD_ERR_UNSUPPORTED;
   if (p.kind == WHEAD_RECURRENT && !p.A) return WHEAD_ERR_UNSUPPORTED;
   if (p.flags & WHEAD_FLAG_W_E4M3) return WHEAD_ERR_UNSUPPORTED;  // needs the handle's quantized copy of W
+  if (p.v_offset < 0 || (p.v_offset & 15)) return WHEAD_ERR_INVALID_ARG;
+  if (p.v_offset + p.V >= (int64_t)1 << 24) return WHEAD_ERR_UNSUPPORTED;
   if (!(T >= 0.0f) || T > 3.0e38f) return WHEAD_ERR_INVALID_ARG;
   if (!aligned16(W) || !aligned16(E) || !aligned16(u0)) return WHEAD_ERR_INVALID_ARG;
   const size_t need = kNaAhOff + 2 * (size_t)kMaxB * p.r * 4;
@@ -721,6 +778,7 @@ extern "C" int whead_walk_noalloc(const void* W, const void* E, const whead_para
   a.ah = reinterpret_cast<float*>(sc + kNaAhOff);
   a.status = out_status ? reinterpret_cast<int*>(out_status) : reinterpret_cast<int*>(sc + kNaStatusOff);
   a.V = p.V;
+  a.v_offset = p.v_offset;
   a.t0 = 0;
   a.seed = seed;
   a.timeout_ns = (uint64_t)(p.timeout_us ? p.timeout_us : 1000000u) * 1000ull;

@@ -32,7 +32,7 @@ ERR_INTERNAL = -6
 # Every symbol include/whead.h declares.
 EXPORTS = ("whead_create", "whead_walk", "whead_walk_ex", "whead_walk_host", "whead_status",
            "whead_plan_info", "whead_strerror", "whead_destroy", "whead_walk_noalloc",
-           "whead_set_trace", "whead_quantize_w_e4m3")
+           "whead_set_trace", "whead_quantize_w_e4m3", "whead_walk_keys", "whead_advance")
 
 
 class WheadParams(ctypes.Structure):
@@ -40,7 +40,8 @@ class WheadParams(ctypes.Structure):
                 ("A", ctypes.c_void_p), ("c", ctypes.c_void_p), ("max_B", ctypes.c_int32),
                 ("max_gamma", ctypes.c_int32), ("stream", ctypes.c_void_p), ("flags", ctypes.c_uint32),
                 ("grid", ctypes.c_int32), ("timeout_us", ctypes.c_uint32), ("cap_smem", ctypes.c_int32),
-                ("cap_tmem", ctypes.c_int32), ("cap_rf", ctypes.c_int32)]
+                ("cap_tmem", ctypes.c_int32), ("cap_rf", ctypes.c_int32), ("v_offset", ctypes.c_int64),
+                ("e_rows", ctypes.c_int64)]
 
 
 class WheadPlan(ctypes.Structure):
@@ -84,9 +85,11 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     L.whead_destroy.argtypes = [vp]
     L.whead_walk_noalloc.argtypes = [vp, vp, ctypes.POINTER(WheadParams), vp, vp, i32, i32, f32, u64, vp, vp, vp]
     L.whead_quantize_w_e4m3.argtypes = [vp, i64, i32, vp, vp, vp]
+    L.whead_walk_keys.argtypes = [vp, vp, vp, i32, i32, f32, u64, i64, vp, vp, vp, vp]
+    L.whead_advance.argtypes = [vp, vp, vp, vp, i32]
     for name in ("whead_create", "whead_walk", "whead_walk_ex", "whead_walk_host", "whead_status",
                  "whead_plan_info", "whead_destroy", "whead_walk_noalloc",
-           "whead_set_trace", "whead_quantize_w_e4m3"):
+                 "whead_set_trace", "whead_quantize_w_e4m3", "whead_walk_keys", "whead_advance"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
@@ -120,11 +123,13 @@ class Head:
     """
 
     def __init__(self, W, E, *, kind=MARKOV, A=None, c=None, max_B=1, max_gamma=16, stream=None, flags=0,
-                 grid=0, timeout_us=0, caps=None):
+                 grid=0, timeout_us=0, caps=None, v_offset=0, e_rows=0):
         import torch
         L = load()
         assert W.is_cuda and W.dtype == torch.bfloat16 and W.is_contiguous() and W.dim() == 2
-        assert E.shape == W.shape and E.dtype == torch.bfloat16 and E.is_contiguous()
+        # E covers the shard's global rows (all of W's rows when the vocabulary is not sharded)
+        assert E.dim() == 2 and E.shape[1] == W.shape[1] and E.shape[0] >= int(v_offset) + W.shape[0]
+        assert E.dtype == torch.bfloat16 and E.is_contiguous()
         self.V, self.r = int(W.shape[0]), int(W.shape[1])
         # caps: (shared, tensor, register) most groups per CTA per tier (placement sweep); the rest stream
         if caps is not None:
@@ -136,7 +141,7 @@ class Head:
         p = WheadParams(kind=self.kind, r=self.r, V=self.V, A=_ptr(A), c=_ptr(c), max_B=int(max_B),
                         max_gamma=int(max_gamma), stream=ctypes.c_void_p(self._stream.cuda_stream),
                         flags=self.flags, grid=int(grid), timeout_us=int(timeout_us), cap_smem=cs, cap_tmem=ct,
-                        cap_rf=cr)
+                        cap_rf=cr, v_offset=int(v_offset), e_rows=int(e_rows))
         h = ctypes.c_void_p()
         _check(L.whead_create(_ptr(W), _ptr(E), ctypes.byref(p), ctypes.byref(h)), "whead_create")
         self._h = h
@@ -157,6 +162,27 @@ class Head:
         _check(load().whead_walk_ex(self._h, _ptr(base), _ptr(s0), B, gamma, float(T), int(seed) & (2**64 - 1),
                                     int(t0), _ptr(out_tokens), _ptr(out_logits), _ptr(out_state)), "whead_walk_ex")
         return out_tokens
+
+    def walk_keys(self, base, s0, *, T=0.0, seed=0, t0=0, out_tokens=None, out_keys=None, out_logits=None,
+                  out_state=None):
+        """whead_walk_ex plus each step's winning packed key: returns (tokens (B, gamma) int32, keys (B, gamma)
+        int64 holding the uint64 keys' bits)."""
+        import torch
+        B, gamma, V = base.shape
+        assert V == self.V and s0.shape == (B, self.r)
+        if out_tokens is None:
+            out_tokens = torch.empty((B, gamma), dtype=torch.int32, device=base.device)
+        if out_keys is None:
+            out_keys = torch.empty((B, gamma), dtype=torch.int64, device=base.device)
+        _check(load().whead_walk_keys(self._h, _ptr(base), _ptr(s0), B, gamma, float(T), int(seed) & (2**64 - 1),
+                                      int(t0), _ptr(out_tokens), _ptr(out_keys), _ptr(out_logits), _ptr(out_state)),
+               "whead_walk_keys")
+        return out_tokens, out_keys
+
+    def advance(self, x, s, s_next):
+        """Next state on the device for winners x (B,) int32 (global rows), from state s (B, r) into s_next."""
+        _check(load().whead_advance(self._h, _ptr(x), _ptr(s), _ptr(s_next), int(x.shape[0])), "whead_advance")
+        return s_next
 
     def walk_host(self, base, u0, *, T=0.0, seed=0, out_tokens=None, out_logits=None):
         """Synchronous walk on host (CPU, ideally pinned) torch tensors; copies are inside the call."""
