@@ -56,7 +56,13 @@ struct whead_s {
   uint32_t parity = 0;
   unsigned long long* trace = nullptr;
   int64_t trace_bytes = 0;
-  // host-call staging
+  // host-call staging; the base logits stream in on copy_stream while the walk runs, step t's arrival marked
+  // by d_ready[t] = ready_gen (copied from h_ready, pinned)
+  cudaStream_t copy_stream = nullptr;
+  cudaEvent_t ev_launch = nullptr;
+  unsigned int* d_ready = nullptr;
+  unsigned int* h_ready = nullptr;
+  unsigned int ready_gen = 0;
   float* d_base = nullptr;
   float* d_u0 = nullptr;
   int32_t* d_tok = nullptr;
@@ -460,8 +466,21 @@ int whead_create(const void* W, const void* E, const whead_params* params, whead
   return WHEAD_OK;
 }
 
+namespace {
+int walk_impl(whead_t* h, const float* base, const float* s0, int32_t B, int32_t gamma, float T, uint64_t seed,
+              int64_t t0, int32_t* out_tokens, uint64_t* out_keys, void* out_logits, float* out_state,
+              const unsigned int* base_ready, unsigned int base_gen);
+}  // namespace
+
 int whead_walk_keys(whead_t* h, const float* base, const float* s0, int32_t B, int32_t gamma, float T, uint64_t seed,
                     int64_t t0, int32_t* out_tokens, uint64_t* out_keys, void* out_logits, float* out_state) {
+  return walk_impl(h, base, s0, B, gamma, T, seed, t0, out_tokens, out_keys, out_logits, out_state, nullptr, 0u);
+}
+
+namespace {
+int walk_impl(whead_t* h, const float* base, const float* s0, int32_t B, int32_t gamma, float T, uint64_t seed,
+              int64_t t0, int32_t* out_tokens, uint64_t* out_keys, void* out_logits, float* out_state,
+              const unsigned int* base_ready, unsigned int base_gen) {
   if (!h || !base || !s0 || !out_tokens) return WHEAD_ERR_INVALID_ARG;
   if (out_keys && (reinterpret_cast<uintptr_t>(out_keys) & 7u)) return WHEAD_ERR_INVALID_ARG;
   if (B < 1 || B > h->p.max_B || gamma < 1 || gamma > h->p.max_gamma || t0 < 0) return WHEAD_ERR_INVALID_ARG;
@@ -480,6 +499,8 @@ int whead_walk_keys(whead_t* h, const float* base, const float* s0, int32_t B, i
   a.A = h->p.A;
   a.c = h->p.c;
   a.base = base;
+  a.base_ready = base_ready;
+  a.base_gen = base_gen;
   a.s0 = s0;
   a.tokens = out_tokens;
   a.keys = reinterpret_cast<unsigned long long*>(out_keys);
@@ -523,6 +544,7 @@ int whead_walk_keys(whead_t* h, const float* base, const float* s0, int32_t B, i
   if (rc == WHEAD_OK) h->parity ^= 1u;
   return rc;
 }
+}  // namespace
 
 int whead_walk_ex(whead_t* h, const float* base, const float* s0, int32_t B, int32_t gamma, float T, uint64_t seed,
                   int64_t t0, int32_t* out_tokens, void* out_logits, float* out_state) {
@@ -560,12 +582,38 @@ int whead_walk_host(whead_t* h, const float* base_host, const float* u0_host, in
     const size_t cap = (size_t)h->p.max_B * h->p.max_gamma * h->p.V;
     if (cudaMalloc(&h->d_logits, cap * logit_elem) != cudaSuccess) return WHEAD_ERR_CUDA;
   }
-  if (cudaMemcpyAsync(h->d_base, base_host, nbase * 4, cudaMemcpyHostToDevice, h->stream) != cudaSuccess)
-    return WHEAD_ERR_CUDA;
+  if (!h->copy_stream) {
+    if (cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking) != cudaSuccess) return WHEAD_ERR_CUDA;
+    if (cudaEventCreateWithFlags(&h->ev_launch, cudaEventDisableTiming) != cudaSuccess) return WHEAD_ERR_CUDA;
+    if (cudaMalloc(&h->d_ready, (size_t)h->p.max_gamma * 4) != cudaSuccess) return WHEAD_ERR_CUDA;
+    if (cudaMemset(h->d_ready, 0, (size_t)h->p.max_gamma * 4) != cudaSuccess) return WHEAD_ERR_CUDA;
+    if (cudaMallocHost(&h->h_ready, (size_t)h->p.max_gamma * 4) != cudaSuccess) return WHEAD_ERR_CUDA;
+  }
+  // this call's flag value (never 0, the flags' initial value); the previous call has finished with h_ready
+  if (++h->ready_gen == 0) h->ready_gen = 1;
+  for (int t = 0; t < gamma; ++t) h->h_ready[t] = h->ready_gen;
+
+  // the walk starts at once; it waits (bounded) for each step's base logits, which stream in behind it in
+  // chunks of 1, 1, then 2 steps, each followed by its steps' ready flags (a chunk lands well within the
+  // time its steps take on the GPU, so the walk rarely waits)
   if (cudaMemcpyAsync(h->d_u0, u0_host, (size_t)B * h->p.r * 4, cudaMemcpyHostToDevice, h->stream) != cudaSuccess)
     return WHEAD_ERR_CUDA;
-  int rc = whead_walk(h, h->d_base, h->d_u0, B, gamma, T, seed, h->d_tok, out_logits_host ? h->d_logits : nullptr);
+  if (cudaEventRecord(h->ev_launch, h->stream) != cudaSuccess) return WHEAD_ERR_CUDA;
+  int rc = walk_impl(h, h->d_base, h->d_u0, B, gamma, T, seed, 0, h->d_tok, nullptr,
+                     out_logits_host ? h->d_logits : nullptr, nullptr, h->d_ready, h->ready_gen);
   if (rc != WHEAD_OK) return rc;
+  if (cudaStreamWaitEvent(h->copy_stream, h->ev_launch, 0) != cudaSuccess) return WHEAD_ERR_CUDA;
+  const size_t pitch = (size_t)gamma * h->p.V * 4;
+  for (int a0 = 0, len = 1; a0 < gamma; a0 += len, len = a0 < 2 ? 1 : 2) {
+    const int n = std::min(len, gamma - a0);
+    const size_t off = (size_t)a0 * h->p.V;
+    if (cudaMemcpy2DAsync(h->d_base + off, pitch, base_host + off, pitch, (size_t)n * h->p.V * 4, (size_t)B,
+                          cudaMemcpyHostToDevice, h->copy_stream) != cudaSuccess)
+      return WHEAD_ERR_CUDA;
+    if (cudaMemcpyAsync(h->d_ready + a0, h->h_ready + a0, (size_t)n * 4, cudaMemcpyHostToDevice, h->copy_stream) !=
+        cudaSuccess)
+      return WHEAD_ERR_CUDA;
+  }
   if (cudaMemcpyAsync(out_tokens_host, h->d_tok, (size_t)B * gamma * 4, cudaMemcpyDeviceToHost, h->stream) !=
       cudaSuccess)
     return WHEAD_ERR_CUDA;
@@ -573,6 +621,7 @@ int whead_walk_host(whead_t* h, const float* base_host, const float* u0_host, in
       cudaMemcpyAsync(out_logits_host, h->d_logits, nbase * logit_elem, cudaMemcpyDeviceToHost, h->stream) != cudaSuccess)
     return WHEAD_ERR_CUDA;
   if (cudaStreamSynchronize(h->stream) != cudaSuccess) return WHEAD_ERR_CUDA;
+  if (cudaStreamSynchronize(h->copy_stream) != cudaSuccess) return WHEAD_ERR_CUDA;
   return WHEAD_OK;
 }
 
@@ -622,6 +671,10 @@ int whead_destroy(whead_t* h) {
   if (h->wq) cudaFree(h->wq);
   if (h->sw) cudaFree(h->sw);
   if (h->d_base) cudaFree(h->d_base);
+  if (h->d_ready) cudaFree(h->d_ready);
+  if (h->h_ready) cudaFreeHost(h->h_ready);
+  if (h->ev_launch) cudaEventDestroy(h->ev_launch);
+  if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
   if (h->d_u0) cudaFree(h->d_u0);
   if (h->d_tok) cudaFree(h->d_tok);
   if (h->d_logits) cudaFree(h->d_logits);

@@ -125,6 +125,27 @@ def test_host_entry_point_matches_device(torch_cuda):
     head.close()
 
 
+def test_host_entry_point_streams_base_logits(torch_cuda):
+    """whead_walk_host starts the walk at once and streams the base logits behind it in chunks of 1, 1, 2, 4
+    and 8 steps; tokens and logits must equal those of the walk on device buffers."""
+    from speculative_decoding_serial_gb300 import whead as wh
+    torch = torch_cuda
+    d = I.make_inputs(O.MARKOV, 20011, 256, 3, 16, seed=33)
+    dd = to_device(d, "cuda")
+    head = wh.Head(dd["W"], dd["E"], kind=O.MARKOV, max_B=3, max_gamma=16, flags=wh.FLAG_LOGITS_F32)
+    lg_dev = torch.empty((3, 16, 20011), dtype=torch.float32, device="cuda")
+    dev_tok = head.walk(dd["base"], dd["s0"], T=1.0, seed=4, out_logits=lg_dev).cpu()
+    base_h = torch.from_numpy(d["base"]).pin_memory()
+    s0_h = torch.from_numpy(d["s0"]).pin_memory()
+    lg_host = torch.empty((3, 16, 20011), dtype=torch.float32).pin_memory()
+    for _ in range(3):  # repeated calls reuse the ready flags with a new generation each time
+        host_tok = head.walk_host(base_h, s0_h, T=1.0, seed=4, out_logits=lg_host)
+        assert torch.equal(dev_tok, host_tok)
+        assert torch.equal(lg_dev.cpu(), lg_host)
+    assert head.status() == 0
+    head.close()
+
+
 def test_wait_limit_reports_timeout_and_context_survives(torch_cuda):
     """CTA 0 skips its first arrival (a host flag); every other CTA's bounded wait must run out."""
     from speculative_decoding_serial_gb300 import whead as wh
