@@ -61,6 +61,8 @@ typedef enum { WHEAD_MARKOV = 0, WHEAD_RECURRENT = 1 } whead_kind;
                                         handle-owned copy (whead_quantize_w_e4m3), and every step splits the state
                                         into two scaled E4M3 vectors whose projections are scaled and summed.
                                         Requires r = 128 or 256 and max_B <= 4; not with whead_walk_noalloc. */
+#define WHEAD_FLAG_HOST_STAGE (1u << 5)  /* whead_walk_host copies the base logits to a device buffer before the walk
+                                           even where the GPU could read the caller's memory in place */
 #define WHEAD_FLAG_FAULT_SKIP_ARRIVAL (1u << 8) /* testing: CTA 0 never arrives at step 0's exchange, so
                                                    every other CTA's bounded wait runs out */
 
@@ -152,9 +154,16 @@ int whead_walk_keys(whead_t* h, const float* base, const float* s0, int32_t B, i
 int whead_advance(whead_t* h, const int32_t* x, const float* s, float* s_next, int32_t B);
 
 /*
- * Synchronous walk on HOST buffers (same arguments as whead_walk, all pointers host memory; pinned
- * memory gives the fastest copies). Copies base and u0 to handle-owned device staging buffers, runs the
- * walk and copies the tokens (and logits, if requested) back, then waits for the stream.
+ * Synchronous walk on HOST buffers (same arguments and layouts as whead_walk; every pointer may be host
+ * memory, pinned or not, and the caller keeps ownership). The base logits (B x gamma x V fp32, about
+ * 9.7 MB for B = 1, gamma = 16, V = 151,936) are read by the walk where they lie whenever this GPU can
+ * address that memory: host memory pinned by CUDA, or any host memory on systems whose GPU walks the
+ * host's page tables (Grace with NVLink-C2C), as well as device or managed memory. Otherwise, or with
+ * WHEAD_FLAG_HOST_STAGE, they are first copied to a handle-owned device buffer. u0 is copied to the device,
+ * the walk runs on the handle's stream, the tokens (and logits, if requested) are copied back, and the call
+ * waits for the stream. Returns WHEAD_OK, an argument or CUDA error, or the first device-side error of the
+ * handle's stream (WHEAD_ERR_TIMEOUT, WHEAD_ERR_INTERNAL), which it then clears as whead_status does; the
+ * outputs are undefined after a device-side error.
  */
 int whead_walk_host(whead_t* h, const float* base_host, const float* u0_host, int32_t B, int32_t gamma,
                     float T, uint64_t seed, int32_t* out_tokens_host, void* out_logits_host);

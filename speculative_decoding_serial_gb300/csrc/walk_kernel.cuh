@@ -64,8 +64,6 @@ struct WalkArgs {
   const float* A;
   const float* c;
   const float* base;
-  const unsigned int* base_ready;  // optional: base logits of step t are in place once base_ready[t] == base_gen
-  unsigned int base_gen;
   const float* s0;
   int32_t* tokens;
   unsigned long long* keys;  // optional: each step's winning packed key per walk, ord(key) << 32 | ~row
@@ -587,40 +585,18 @@ __device__ __forceinline__ void bfrag_from_bf16_row(uint32_t (&bf)[KB][8], const
 }
 
 // Copies the base logits of step t for this CTA's rows into shared memory (coalesced; rows >= V read as
-// zero) using threads [first, first + count), and asks L2 for the rows of step t + 1.
-// When the base logits arrive while the walk runs (host-buffer calls copy them step by step on another
-// stream), each participating warp first waits, bounded, for step t's ready flag; running out of time sets
-// the time-out status and the abort flag and stages nothing. The copy uses L2-coherent loads on both paths
-// (the base logits are read once, so the read-only path gains nothing).
+// zero) using threads [first, first + count), and asks L2 for the rows of step t + 1. The base logits may
+// sit in host memory that the GPU reads in place; the L2 request one step ahead hides that latency too.
 __device__ __forceinline__ void stage_base(const WalkArgs& P, float* s_base, int64_t row_base, int t, int first,
-                                           int count, volatile int* s_abort) {
+                                           int count) {
   const int rows = P.ng * kGroupRows;
   const int i0 = (int)threadIdx.x - first;
   if (i0 < 0 || i0 >= count || t >= P.gamma) return;
-  if (P.base_ready != nullptr) {
-    bool ready = true;
-    if ((threadIdx.x & 31) == 0) {
-      const uint64_t t_start = globaltimer_ns();
-      uint32_t spins = 0;
-      while (true) {
-        unsigned int v;
-        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(P.base_ready + t) : "memory");
-        if (v == P.base_gen) break;
-        if ((++spins & 15u) == 0u && globaltimer_ns() - t_start > P.timeout_ns) {
-          atomicCAS(P.status, 0, kStatusTimeout);
-          *s_abort = 1;
-          ready = false;
-          break;
-        }
-      }
-    }
-    if (!__shfl_sync(0xffffffffu, ready, 0)) return;
-  }
   const int valid = (int)min((int64_t)rows, P.V - row_base);  // rows of this CTA below V (may be <= 0)
   for (int n = 0; n < P.B; ++n) {
     const float* src = P.base + ((int64_t)n * P.gamma + t) * P.V + row_base;
     float* dst = s_base + n * rows;
-    for (int lr = i0; lr < rows; lr += count) dst[lr] = (lr < valid) ? __ldcg(src + lr) : 0.f;
+    for (int lr = i0; lr < rows; lr += count) dst[lr] = (lr < valid) ? __ldg(src + lr) : 0.f;
     if (t + 1 < P.gamma)
       for (int lr = 32 * i0; lr < valid; lr += 32 * count) prefetch_l2(src + P.V + lr);
   }
@@ -724,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  stage_base(P, s_base, row_base, 0, 0, kThreads, s_abort);
+  stage_base(P, s_base, row_base, 0, 0, kThreads);
 
   // tensor-memory groups of this warp: global -> registers (all boxes of a group in flight) -> tcgen05.st
   if (!rf_warp) {
@@ -1109,7 +1085,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       trace_stamp(P, 2 + kTraceStampsPerStep * t + 1);
 
       // the other warps fetch the next step's base logits while warp 0 runs the exchange
-      stage_base(P, s_base, row_base, t + 1, 32, kThreads - 32, s_abort);
+      stage_base(P, s_base, row_base, t + 1, 32, kThreads - 32);
 
       // exchange (Fig. 8). Each CTA publishes its winner for walk n as one 64-bit word in its own slot,
       // tag (step + 1) << 56 | ord(key) << 24 | (2^24 - 1 - row), with a relaxed store: an aligned 64-bit store

@@ -56,13 +56,9 @@ struct whead_s {
   uint32_t parity = 0;
   unsigned long long* trace = nullptr;
   int64_t trace_bytes = 0;
-  // host-call staging; the base logits stream in on copy_stream while the walk runs, step t's arrival marked
-  // by d_ready[t] = ready_gen (copied from h_ready, pinned)
-  cudaStream_t copy_stream = nullptr;
-  cudaEvent_t ev_launch = nullptr;
-  unsigned int* d_ready = nullptr;
-  unsigned int* h_ready = nullptr;
-  unsigned int ready_gen = 0;
+  // host-call staging (d_base only for base logits the GPU cannot read in place) and the status read-back
+  int pageable_access = 0;  // the GPU reads any host memory through the host's page tables
+  int* h_status = nullptr;  // pinned
   float* d_base = nullptr;
   float* d_u0 = nullptr;
   int32_t* d_tok = nullptr;
@@ -408,6 +404,8 @@ int whead_create(const void* W, const void* E, const whead_params* params, whead
   int coop = 0;
   if (cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, h->device) != cudaSuccess || !coop)
     return fail(WHEAD_ERR_NO_COOP);
+  if (cudaDeviceGetAttribute(&h->pageable_access, cudaDevAttrPageableMemoryAccess, h->device) != cudaSuccess)
+    return fail(WHEAD_ERR_CUDA);
 
   h->slots_per_parity = 2 * (int64_t)h->sm_count * kMaxB;
 
@@ -468,19 +466,17 @@ int whead_create(const void* W, const void* E, const whead_params* params, whead
 
 namespace {
 int walk_impl(whead_t* h, const float* base, const float* s0, int32_t B, int32_t gamma, float T, uint64_t seed,
-              int64_t t0, int32_t* out_tokens, uint64_t* out_keys, void* out_logits, float* out_state,
-              const unsigned int* base_ready, unsigned int base_gen);
+              int64_t t0, int32_t* out_tokens, uint64_t* out_keys, void* out_logits, float* out_state);
 }  // namespace
 
 int whead_walk_keys(whead_t* h, const float* base, const float* s0, int32_t B, int32_t gamma, float T, uint64_t seed,
                     int64_t t0, int32_t* out_tokens, uint64_t* out_keys, void* out_logits, float* out_state) {
-  return walk_impl(h, base, s0, B, gamma, T, seed, t0, out_tokens, out_keys, out_logits, out_state, nullptr, 0u);
+  return walk_impl(h, base, s0, B, gamma, T, seed, t0, out_tokens, out_keys, out_logits, out_state);
 }
 
 namespace {
 int walk_impl(whead_t* h, const float* base, const float* s0, int32_t B, int32_t gamma, float T, uint64_t seed,
-              int64_t t0, int32_t* out_tokens, uint64_t* out_keys, void* out_logits, float* out_state,
-              const unsigned int* base_ready, unsigned int base_gen) {
+              int64_t t0, int32_t* out_tokens, uint64_t* out_keys, void* out_logits, float* out_state) {
   if (!h || !base || !s0 || !out_tokens) return WHEAD_ERR_INVALID_ARG;
   if (out_keys && (reinterpret_cast<uintptr_t>(out_keys) & 7u)) return WHEAD_ERR_INVALID_ARG;
   if (B < 1 || B > h->p.max_B || gamma < 1 || gamma > h->p.max_gamma || t0 < 0) return WHEAD_ERR_INVALID_ARG;
@@ -499,8 +495,6 @@ int walk_impl(whead_t* h, const float* base, const float* s0, int32_t B, int32_t
   a.A = h->p.A;
   a.c = h->p.c;
   a.base = base;
-  a.base_ready = base_ready;
-  a.base_gen = base_gen;
   a.s0 = s0;
   a.tokens = out_tokens;
   a.keys = reinterpret_cast<unsigned long long*>(out_keys);
@@ -566,63 +560,73 @@ int whead_advance(whead_t* h, const int32_t* x, const float* s, float* s_next, i
   return cudaGetLastError() == cudaSuccess ? WHEAD_OK : WHEAD_ERR_CUDA;
 }
 
+namespace {
+// A pointer this GPU can read the caller's memory through, or nullptr: memory of this device, managed
+// memory, host memory pinned and mapped by CUDA, or any host memory where the GPU walks the host's page
+// tables (as on Grace over NVLink-C2C).
+const float* device_view(const whead_t* h, const float* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  switch (at.type) {
+    case cudaMemoryTypeDevice: return at.device == h->device ? p : nullptr;
+    case cudaMemoryTypeManaged: return p;
+    case cudaMemoryTypeHost: return static_cast<const float*>(at.devicePointer);
+    default: return h->pageable_access ? p : nullptr;
+  }
+}
+}  // namespace
+
 int whead_walk_host(whead_t* h, const float* base_host, const float* u0_host, int32_t B, int32_t gamma, float T,
                     uint64_t seed, int32_t* out_tokens_host, void* out_logits_host) {
   if (!h || !base_host || !u0_host || !out_tokens_host) return WHEAD_ERR_INVALID_ARG;
   if (B < 1 || B > h->p.max_B || gamma < 1 || gamma > h->p.max_gamma) return WHEAD_ERR_INVALID_ARG;
   const size_t nbase = (size_t)B * gamma * h->p.V;
   const size_t logit_elem = (h->p.flags & WHEAD_FLAG_LOGITS_F32) ? 4 : 2;
-  if (!h->d_base) {
-    const size_t cap = (size_t)h->p.max_B * h->p.max_gamma * h->p.V;
-    if (cudaMalloc(&h->d_base, cap * 4) != cudaSuccess) return WHEAD_ERR_CUDA;
+  if (!h->d_u0) {
     if (cudaMalloc(&h->d_u0, (size_t)h->p.max_B * h->p.r * 4) != cudaSuccess) return WHEAD_ERR_CUDA;
     if (cudaMalloc(&h->d_tok, (size_t)h->p.max_B * h->p.max_gamma * 4) != cudaSuccess) return WHEAD_ERR_CUDA;
+    if (cudaMallocHost(&h->h_status, sizeof(int)) != cudaSuccess) return WHEAD_ERR_CUDA;
   }
   if (out_logits_host && !h->d_logits) {
     const size_t cap = (size_t)h->p.max_B * h->p.max_gamma * h->p.V;
     if (cudaMalloc(&h->d_logits, cap * logit_elem) != cudaSuccess) return WHEAD_ERR_CUDA;
   }
-  if (!h->copy_stream) {
-    if (cudaStreamCreateWithFlags(&h->copy_stream, cudaStreamNonBlocking) != cudaSuccess) return WHEAD_ERR_CUDA;
-    if (cudaEventCreateWithFlags(&h->ev_launch, cudaEventDisableTiming) != cudaSuccess) return WHEAD_ERR_CUDA;
-    if (cudaMalloc(&h->d_ready, (size_t)h->p.max_gamma * 4) != cudaSuccess) return WHEAD_ERR_CUDA;
-    if (cudaMemset(h->d_ready, 0, (size_t)h->p.max_gamma * 4) != cudaSuccess) return WHEAD_ERR_CUDA;
-    if (cudaMallocHost(&h->h_ready, (size_t)h->p.max_gamma * 4) != cudaSuccess) return WHEAD_ERR_CUDA;
+  // the walk reads each step's base logits where the caller keeps them when the GPU can address that memory
+  // (the kernel asks L2 for step t + 1's rows during step t, which hides the host link's latency); otherwise
+  // they are copied to a device buffer first
+  const float* base = (h->p.flags & WHEAD_FLAG_HOST_STAGE) ? nullptr : device_view(h, base_host);
+  if (!base) {
+    if (!h->d_base) {
+      const size_t cap = (size_t)h->p.max_B * h->p.max_gamma * h->p.V;
+      if (cudaMalloc(&h->d_base, cap * 4) != cudaSuccess) return WHEAD_ERR_CUDA;
+    }
+    if (cudaMemcpyAsync(h->d_base, base_host, nbase * 4, cudaMemcpyDefault, h->stream) != cudaSuccess)
+      return WHEAD_ERR_CUDA;
+    base = h->d_base;
   }
-  // this call's flag value (never 0, the flags' initial value); the previous call has finished with h_ready
-  if (++h->ready_gen == 0) h->ready_gen = 1;
-  for (int t = 0; t < gamma; ++t) h->h_ready[t] = h->ready_gen;
-
-  // the walk starts at once; it waits (bounded) for each step's base logits, which stream in behind it in
-  // chunks of 1, 1, then 2 steps, each followed by its steps' ready flags (a chunk lands well within the
-  // time its steps take on the GPU, so the walk rarely waits)
-  if (cudaMemcpyAsync(h->d_u0, u0_host, (size_t)B * h->p.r * 4, cudaMemcpyHostToDevice, h->stream) != cudaSuccess)
+  if (cudaMemcpyAsync(h->d_u0, u0_host, (size_t)B * h->p.r * 4, cudaMemcpyDefault, h->stream) != cudaSuccess)
     return WHEAD_ERR_CUDA;
-  if (cudaEventRecord(h->ev_launch, h->stream) != cudaSuccess) return WHEAD_ERR_CUDA;
-  int rc = walk_impl(h, h->d_base, h->d_u0, B, gamma, T, seed, 0, h->d_tok, nullptr,
-                     out_logits_host ? h->d_logits : nullptr, nullptr, h->d_ready, h->ready_gen);
+  const int rc = walk_impl(h, base, h->d_u0, B, gamma, T, seed, 0, h->d_tok, nullptr,
+                           out_logits_host ? h->d_logits : nullptr, nullptr);
   if (rc != WHEAD_OK) return rc;
-  if (cudaStreamWaitEvent(h->copy_stream, h->ev_launch, 0) != cudaSuccess) return WHEAD_ERR_CUDA;
-  const size_t pitch = (size_t)gamma * h->p.V * 4;
-  for (int a0 = 0, len = 1; a0 < gamma; a0 += len, len = a0 < 2 ? 1 : 2) {
-    const int n = std::min(len, gamma - a0);
-    const size_t off = (size_t)a0 * h->p.V;
-    if (cudaMemcpy2DAsync(h->d_base + off, pitch, base_host + off, pitch, (size_t)n * h->p.V * 4, (size_t)B,
-                          cudaMemcpyHostToDevice, h->copy_stream) != cudaSuccess)
-      return WHEAD_ERR_CUDA;
-    if (cudaMemcpyAsync(h->d_ready + a0, h->h_ready + a0, (size_t)n * 4, cudaMemcpyHostToDevice, h->copy_stream) !=
-        cudaSuccess)
-      return WHEAD_ERR_CUDA;
-  }
-  if (cudaMemcpyAsync(out_tokens_host, h->d_tok, (size_t)B * gamma * 4, cudaMemcpyDeviceToHost, h->stream) !=
+  if (cudaMemcpyAsync(out_tokens_host, h->d_tok, (size_t)B * gamma * 4, cudaMemcpyDefault, h->stream) !=
       cudaSuccess)
     return WHEAD_ERR_CUDA;
   if (out_logits_host &&
-      cudaMemcpyAsync(out_logits_host, h->d_logits, nbase * logit_elem, cudaMemcpyDeviceToHost, h->stream) != cudaSuccess)
+      cudaMemcpyAsync(out_logits_host, h->d_logits, nbase * logit_elem, cudaMemcpyDefault, h->stream) != cudaSuccess)
+    return WHEAD_ERR_CUDA;
+  if (cudaMemcpyAsync(h->h_status, h->s.status, sizeof(int), cudaMemcpyDeviceToHost, h->stream) != cudaSuccess)
     return WHEAD_ERR_CUDA;
   if (cudaStreamSynchronize(h->stream) != cudaSuccess) return WHEAD_ERR_CUDA;
-  if (cudaStreamSynchronize(h->copy_stream) != cudaSuccess) return WHEAD_ERR_CUDA;
-  return WHEAD_OK;
+  const int st = *h->h_status;
+  if (st != 0) {  // report the device-side error once, as whead_status does
+    if (cudaMemsetAsync(h->s.status, 0, sizeof(int), h->stream) != cudaSuccess) return WHEAD_ERR_CUDA;
+    if (cudaStreamSynchronize(h->stream) != cudaSuccess) return WHEAD_ERR_CUDA;
+  }
+  return st;
 }
 
 int whead_set_trace(whead_t* h, void* trace, int64_t bytes) {
@@ -671,10 +675,7 @@ int whead_destroy(whead_t* h) {
   if (h->wq) cudaFree(h->wq);
   if (h->sw) cudaFree(h->sw);
   if (h->d_base) cudaFree(h->d_base);
-  if (h->d_ready) cudaFree(h->d_ready);
-  if (h->h_ready) cudaFreeHost(h->h_ready);
-  if (h->ev_launch) cudaEventDestroy(h->ev_launch);
-  if (h->copy_stream) cudaStreamDestroy(h->copy_stream);
+  if (h->h_status) cudaFreeHost(h->h_status);
   if (h->d_u0) cudaFree(h->d_u0);
   if (h->d_tok) cudaFree(h->d_tok);
   if (h->d_logits) cudaFree(h->d_logits);

@@ -19,6 +19,7 @@ FLAG_FIXED_LATENT = 1 << 1
 FLAG_FORCE_STREAM = 1 << 2
 FLAG_PLACEMENT_CAPS = 1 << 3
 FLAG_W_E4M3 = 1 << 4
+FLAG_HOST_STAGE = 1 << 5
 FLAG_FAULT_SKIP_ARRIVAL = 1 << 8
 
 OK = 0
@@ -185,7 +186,9 @@ class Head:
         return s_next
 
     def walk_host(self, base, u0, *, T=0.0, seed=0, out_tokens=None, out_logits=None):
-        """Synchronous walk on host (CPU, ideally pinned) torch tensors; copies are inside the call."""
+        """Synchronous walk on host (CPU) torch tensors. The walk reads the base logits in place where the GPU
+        can address them (pinned memory; any host memory on Grace); u0 and the outputs are copied inside the
+        call. Raises on a device-side error of the walk."""
         import torch
         B, gamma, V = base.shape
         assert V == self.V and not base.is_cuda and not u0.is_cuda

@@ -125,25 +125,48 @@ def test_host_entry_point_matches_device(torch_cuda):
     head.close()
 
 
-def test_host_entry_point_streams_base_logits(torch_cuda):
-    """whead_walk_host starts the walk at once and streams the base logits behind it in chunks of 1, 1, 2, 4
-    and 8 steps; tokens and logits must equal those of the walk on device buffers."""
+@pytest.mark.parametrize("memory", ["pinned", "pageable", "staged"])
+def test_host_entry_point_base_in_place_or_staged(torch_cuda, memory):
+    """whead_walk_host reads the base logits where they lie when the GPU can address them (pinned memory; any
+    host memory where the GPU walks the host's page tables) and copies them first otherwise or when asked to
+    (FLAG_HOST_STAGE); tokens and logits must equal those of the walk on device buffers, call after call."""
     from speculative_decoding_serial_gb300 import whead as wh
     torch = torch_cuda
     d = I.make_inputs(O.MARKOV, 20011, 256, 3, 16, seed=33)
     dd = to_device(d, "cuda")
-    head = wh.Head(dd["W"], dd["E"], kind=O.MARKOV, max_B=3, max_gamma=16, flags=wh.FLAG_LOGITS_F32)
+    flags = wh.FLAG_LOGITS_F32 | (wh.FLAG_HOST_STAGE if memory == "staged" else 0)
+    head = wh.Head(dd["W"], dd["E"], kind=O.MARKOV, max_B=3, max_gamma=16, flags=flags)
     lg_dev = torch.empty((3, 16, 20011), dtype=torch.float32, device="cuda")
     dev_tok = head.walk(dd["base"], dd["s0"], T=1.0, seed=4, out_logits=lg_dev).cpu()
-    base_h = torch.from_numpy(d["base"]).pin_memory()
-    s0_h = torch.from_numpy(d["s0"]).pin_memory()
-    lg_host = torch.empty((3, 16, 20011), dtype=torch.float32).pin_memory()
-    for _ in range(3):  # repeated calls reuse the ready flags with a new generation each time
+    base_h = torch.from_numpy(d["base"])
+    s0_h = torch.from_numpy(d["s0"])
+    lg_host = torch.empty((3, 16, 20011), dtype=torch.float32)
+    if memory == "pinned":
+        base_h, s0_h, lg_host = base_h.pin_memory(), s0_h.pin_memory(), lg_host.pin_memory()
+    for k in range(3):
+        if k == 2:
+            base_h = base_h.clone()  # a different buffer on the last call
+            base_h = base_h.pin_memory() if memory == "pinned" else base_h
         host_tok = head.walk_host(base_h, s0_h, T=1.0, seed=4, out_logits=lg_host)
         assert torch.equal(dev_tok, host_tok)
         assert torch.equal(lg_dev.cpu(), lg_host)
     assert head.status() == 0
     head.close()
+
+
+def test_host_entry_point_reports_device_errors(torch_cuda):
+    """A walk whose bounded waits run out makes whead_walk_host return WHEAD_ERR_TIMEOUT (and clear it)."""
+    from speculative_decoding_serial_gb300 import whead as wh
+    torch = torch_cuda
+    d = I.make_inputs(O.MARKOV, 40000, 128, 1, 3, seed=2)
+    dd = to_device(d, "cuda")
+    bad = wh.Head(dd["W"], dd["E"], kind=O.MARKOV, max_B=1, max_gamma=3, flags=wh.FLAG_FAULT_SKIP_ARRIVAL,
+                  timeout_us=20000)
+    with pytest.raises(wh.WheadError) as err:
+        bad.walk_host(torch.from_numpy(d["base"]), torch.from_numpy(d["s0"]))
+    assert err.value.code == wh.ERR_TIMEOUT
+    assert bad.status() == 0
+    bad.close()
 
 
 def test_wait_limit_reports_timeout_and_context_survives(torch_cuda):
