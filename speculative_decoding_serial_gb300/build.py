@@ -9,14 +9,16 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libwhead.so")
-SOURCES = [os.path.join(CSRC, "whead_api.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, "walk_kernel.cuh"), os.path.join(ROOT, "include", "whead.h")]
+# the host library and the two halves of the walk kernel's instantiations, compiled in parallel
+SOURCES = [os.path.join(CSRC, n) for n in ("whead_api.cu", "walk_resident.cu", "walk_async.cu")]
+DEPS = SOURCES + [os.path.join(CSRC, n) for n in ("walk_kernel.cuh", "walk_launch.cuh", "walk_launch.h")] + [
+    os.path.join(ROOT, "include", "whead.h")]
 # measurement-only library used by the benchmark for the roofline's on-chip figures
 PROBE_LIB = os.path.join(BUILD, "libwhead_probe.so")
 PROBE_SRC = os.path.join(CSRC, "onchip_probe.cu")
 
 NVCC_FLAGS = ["-O3", "-std=c++17", "-gencode", "arch=compute_103a,code=sm_103a", "-lineinfo",
-              "-Xcompiler", "-fPIC", "-shared", "-Xptxas", "-v"]
+              "-Xcompiler", "-fPIC", "-Xptxas", "-v"]
 
 
 def nvcc() -> str:
@@ -32,15 +34,34 @@ def needs_build() -> bool:
 
 
 def _compile(out: str, sources, log_name: str, verbose: bool) -> None:
-    tmp = out + f".tmp{os.getpid()}"
-    cmd = [nvcc()] + NVCC_FLAGS + ["-I", os.path.join(ROOT, "include"), "-o", tmp] + list(sources)
-    res = subprocess.run(cmd, capture_output=True, text=True)
-    if res.returncode != 0:
-        raise RuntimeError("nvcc failed:\n" + res.stdout + res.stderr)
+    """Each source to an object file (all at once, one nvcc process per source), then one shared library."""
+    tag = f".tmp{os.getpid()}"
+    objs = [os.path.join(BUILD, os.path.splitext(os.path.basename(src))[0] + tag + ".o") for src in sources]
+    procs = [subprocess.Popen([nvcc()] + NVCC_FLAGS + ["-I", os.path.join(ROOT, "include"), "-c", "-o", obj, src],
+                              stdout=subprocess.PIPE, stderr=subprocess.PIPE, text=True)
+             for src, obj in zip(sources, objs)]
+    logs, failed = [], []
+    for src, p in zip(sources, procs):
+        o, e = p.communicate()
+        logs.append(e)
+        if p.returncode != 0:
+            failed.append(f"{os.path.basename(src)}:\n{o}{e}")
+    try:
+        if failed:
+            raise RuntimeError("nvcc failed:\n" + "\n".join(failed))
+        tmp = out + tag
+        res = subprocess.run([nvcc(), "-shared", "-gencode", "arch=compute_103a,code=sm_103a", "-o", tmp] + objs,
+                             capture_output=True, text=True)
+        if res.returncode != 0:
+            raise RuntimeError("nvcc link failed:\n" + res.stdout + res.stderr)
+    finally:
+        for obj in objs:
+            if os.path.exists(obj):
+                os.remove(obj)
     with open(os.path.join(BUILD, log_name), "w") as f:
-        f.write(res.stderr)
+        f.write("".join(logs))
     if verbose:
-        print(res.stderr)
+        print("".join(logs))
     os.replace(tmp, out)
 
 

@@ -56,6 +56,7 @@ constexpr uint32_t kFlagLogitsF32 = 1u << 0;
 constexpr uint32_t kFlagFixedLatent = 1u << 1;
 constexpr uint32_t kFlagForceStream = 1u << 2;
 constexpr uint32_t kFlagSkipArrival = 1u << 8;
+constexpr uint32_t kFlagBaseAsync = 1u << 24;  // set by the library: next step's base logits copied during a step
 
 struct WalkArgs {
   const uint16_t* W;  // rows of rw 16-bit words: bf16 values, or (E4M3 weights) pairs of 8-bit codes
@@ -129,6 +130,8 @@ struct SmemLayout {
   }
 };
 
+// Shared memory for the incoming base-logit buffer of asynchronous base copies (16 bytes of alignment slack).
+__host__ __device__ inline int base_in_bytes(int B, int ng) { return 16 + B * ng * kGroupRows * 4; }
 
 // ------------------------------------------------------------------------------------------------
 // small device helpers
@@ -602,6 +605,39 @@ __device__ __forceinline__ void stage_base(const WalkArgs& P, float* s_base, int
   }
 }
 
+// The same rows as stage_base, copied asynchronously into a second buffer (cp.async, 4 bytes per row; the
+// group is committed here and waited for by the same thread with cp.async.wait_all). Used when the base
+// logits sit behind a slow link (host memory read in place): the copy for step t + 2 is issued during step t,
+// so a whole step passes before its rows are needed.
+__device__ __forceinline__ void copy_base_async(const WalkArgs& P, float* s_dst, int64_t row_base, int t, int first,
+                                                int count) {
+  const int rows = P.ng * kGroupRows;
+  const int i0 = (int)threadIdx.x - first;
+  if (i0 < 0 || i0 >= count || t >= P.gamma) return;
+  const int valid = (int)min((int64_t)rows, P.V - row_base);
+  for (int n = 0; n < P.B; ++n) {
+    const float* src = P.base + ((int64_t)n * P.gamma + t) * P.V + row_base;
+    float* dst = s_dst + n * rows;
+    for (int lr = i0; lr < rows; lr += count) {
+      if (lr < valid)
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst + lr)), "l"(src + lr) : "memory");
+      else
+        dst[lr] = 0.f;
+    }
+  }
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Each thread moves the rows it copied with copy_base_async (same partition) into this step's buffer.
+__device__ __forceinline__ void move_base(const WalkArgs& P, float* s_base, const float* s_in, int t, int first,
+                                          int count) {
+  const int rows = P.ng * kGroupRows;
+  const int i0 = (int)threadIdx.x - first;
+  if (i0 < 0 || i0 >= count || t >= P.gamma) return;
+  for (int n = 0; n < P.B; ++n)
+    for (int lr = i0; lr < rows; lr += count) s_base[n * rows + lr] = s_in[n * rows + lr];
+}
+
 // ------------------------------------------------------------------------------------------------
 // the kernel
 // ------------------------------------------------------------------------------------------------
@@ -609,7 +645,9 @@ __device__ __forceinline__ void stage_base(const WalkArgs& P, float* s_base, int
 // Warp roles: warps in rf_warp_mask keep one group in registers (plus shared-memory groups); the others
 // own the tensor-memory groups of their lane quadrant (plus shared-memory groups). The two roles run
 // separately compiled copies of the step loop so that neither pays for the other's registers.
-template <int KB, int NH, bool NB1, bool F8>
+// F8: E4M3 weights. ASYNC: each step's base logits are copied asynchronously a step ahead into a second
+// buffer (walks that read them from host memory); kept out of the other variants' step loop.
+template <int KB, int NH, bool NB1, bool F8, bool ASYNC>
 __global__ void __launch_bounds__(kThreads, 1)
     walk_kernel(const __grid_constant__ CUtensorMap tmapW, const __grid_constant__ CUtensorMap tmapW128,
                 const __grid_constant__ WalkArgs P) {
@@ -631,6 +669,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + L.misc + 8);
   volatile int* s_abort = reinterpret_cast<volatile int*>(smem + L.misc + 12);
   float* s_base = reinterpret_cast<float*>(smem + L.base);
+  // with asynchronous base copies, a second buffer past the end of the layout receives the step after next
+  constexpr bool base_async = ASYNC;  // launched with kFlagBaseAsync set
+  float* s_base_in = reinterpret_cast<float*>(smem + ((L.total + 15) & ~15));
   float* s_h = reinterpret_cast<float*>(smem + L.h);
   float* s_A = reinterpret_cast<float*>(smem + L.a);
   float* s_sw = reinterpret_cast<float*>(smem + L.sw);  // E4M3 weights: scales of this CTA's rows
@@ -701,6 +742,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   stage_base(P, s_base, row_base, 0, 0, kThreads);
+  if constexpr (base_async) copy_base_async(P, s_base_in, row_base, 1, 32, kThreads - 32);
 
   // tensor-memory groups of this warp: global -> registers (all boxes of a group in flight) -> tcgen05.st
   if (!rf_warp) {
@@ -1084,8 +1126,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncthreads();
       trace_stamp(P, 2 + kTraceStampsPerStep * t + 1);
 
-      // the other warps fetch the next step's base logits while warp 0 runs the exchange
-      stage_base(P, s_base, row_base, t + 1, 32, kThreads - 32);
+      // the other warps fetch the next step's base logits while warp 0 runs the exchange; with asynchronous
+      // copies each thread takes the rows it had copied a step earlier and starts the copy for the step after
+      if constexpr (base_async) {
+        if (tid >= 32) {
+          asm volatile("cp.async.wait_all;" ::: "memory");
+          move_base(P, s_base, s_base_in, t + 1, 32, kThreads - 32);
+          copy_base_async(P, s_base_in, row_base, t + 2, 32, kThreads - 32);
+        }
+      } else {
+        stage_base(P, s_base, row_base, t + 1, 32, kThreads - 32);
+      }
 
       // exchange (Fig. 8). Each CTA publishes its winner for walk n as one 64-bit word in its own slot,
       // tag (step + 1) << 56 | ord(key) << 24 | (2^24 - 1 - row), with a relaxed store: an aligned 64-bit store
@@ -1284,6 +1335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------- exit ----------------
   // copies still in flight after a timed-out wait must land before the CTA's shared memory is released
   if (!tma_done) (void)mbar_wait_bounded(mbar, 0u, P.timeout_ns);
+  if constexpr (base_async) asm volatile("cp.async.wait_all;" ::: "memory");
   tmem_fence_before();
   __syncthreads();
   tmem_fence_after();

@@ -5,6 +5,7 @@
 // gives each SM an equal run of groups and places them in shared memory, tensor memory and registers.
 #include "../../include/whead.h"
 #include "walk_kernel.cuh"
+#include "walk_launch.h"
 
 #include <cudaTypedefs.h>
 
@@ -201,57 +202,9 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return fn;
 }
 
-template <int KB, int NH, bool NB1, bool F8 = false>
-int launch_t(whead_t* h, const Plan& pl, const WalkArgs& a) {
-  auto fn = walk_kernel<KB, NH, NB1, F8>;
-  static int attr_bytes = 0;  // largest dynamic shared memory size granted so far (per instantiation)
-  if (pl.smem_bytes > attr_bytes) {
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, h->smem_optin) != cudaSuccess)
-      return WHEAD_ERR_CUDA;
-    attr_bytes = h->smem_optin;
-  }
-  void* args[] = {(void*)&h->tmap, (void*)&h->tmap128, (void*)&a};
-  cudaError_t e = cudaLaunchCooperativeKernel((const void*)fn, dim3(pl.G), dim3(kThreads), args, (size_t)pl.smem_bytes,
-                                              h->stream);
-  if (e == cudaErrorCooperativeLaunchTooLarge) {
-    (void)cudaGetLastError();
-    return WHEAD_ERR_NO_COOP;
-  }
-  if (e != cudaSuccess) {
-    (void)cudaGetLastError();
-    return WHEAD_ERR_CUDA;
-  }
-  return WHEAD_OK;
-}
-
-// Instantiation for (rank boxes, batch halves, single walk).
 int launch(whead_t* h, const Plan& pl, const WalkArgs& a, int NH) {
-  const bool one = a.B == 1;
-  if (h->f8) {  // E4M3 weights: one batch half (at most 4 walks), r = 128 or 256
-    switch (kb_of(h->p.r, true) * 2 + (one ? 1 : 0)) {
-      case 2: return launch_t<1, 1, false, true>(h, pl, a);
-      case 3: return launch_t<1, 1, true, true>(h, pl, a);
-      case 4: return launch_t<2, 1, false, true>(h, pl, a);
-      case 5: return launch_t<2, 1, true, true>(h, pl, a);
-      default: return WHEAD_ERR_UNSUPPORTED;
-    }
-  }
-  const int KB = kb_of(h->p.r);
-  switch (KB * 4 + (NH - 1) * 2 + (one ? 1 : 0)) {
-    case 4: return launch_t<1, 1, false>(h, pl, a);
-    case 5: return launch_t<1, 1, true>(h, pl, a);
-    case 6: return launch_t<1, 2, false>(h, pl, a);
-    case 8: return launch_t<2, 1, false>(h, pl, a);
-    case 9: return launch_t<2, 1, true>(h, pl, a);
-    case 10: return launch_t<2, 2, false>(h, pl, a);
-    case 12: return launch_t<3, 1, false>(h, pl, a);
-    case 13: return launch_t<3, 1, true>(h, pl, a);
-    case 14: return launch_t<3, 2, false>(h, pl, a);
-    case 16: return launch_t<4, 1, false>(h, pl, a);
-    case 17: return launch_t<4, 1, true>(h, pl, a);
-    case 18: return launch_t<4, 2, false>(h, pl, a);
-    default: return WHEAD_ERR_UNSUPPORTED;
-  }
+  const WalkLaunch l{&h->tmap, &h->tmap128, h->stream, h->smem_optin, pl.G, pl.smem_bytes, h->p.r, NH, h->f8};
+  return (a.flags & kFlagBaseAsync) ? launch_walk_async(l, a) : launch_walk_resident(l, a);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -466,7 +419,8 @@ int whead_create(const void* W, const void* E, const whead_params* params, whead
 
 namespace {
 int walk_impl(whead_t* h, const float* base, const float* s0, int32_t B, int32_t gamma, float T, uint64_t seed,
-              int64_t t0, int32_t* out_tokens, uint64_t* out_keys, void* out_logits, float* out_state);
+              int64_t t0, int32_t* out_tokens, uint64_t* out_keys, void* out_logits, float* out_state,
+              bool base_async = false);
 }  // namespace
 
 int whead_walk_keys(whead_t* h, const float* base, const float* s0, int32_t B, int32_t gamma, float T, uint64_t seed,
@@ -476,7 +430,8 @@ int whead_walk_keys(whead_t* h, const float* base, const float* s0, int32_t B, i
 
 namespace {
 int walk_impl(whead_t* h, const float* base, const float* s0, int32_t B, int32_t gamma, float T, uint64_t seed,
-              int64_t t0, int32_t* out_tokens, uint64_t* out_keys, void* out_logits, float* out_state) {
+              int64_t t0, int32_t* out_tokens, uint64_t* out_keys, void* out_logits, float* out_state,
+              bool base_async) {
   if (!h || !base || !s0 || !out_tokens) return WHEAD_ERR_INVALID_ARG;
   if (out_keys && (reinterpret_cast<uintptr_t>(out_keys) & 7u)) return WHEAD_ERR_INVALID_ARG;
   if (B < 1 || B > h->p.max_B || gamma < 1 || gamma > h->p.max_gamma || t0 < 0) return WHEAD_ERR_INVALID_ARG;
@@ -522,7 +477,9 @@ int walk_impl(whead_t* h, const float* base, const float* s0, int32_t B, int32_t
   a.B = B;
   a.gamma = gamma;
   a.kind = h->p.kind;
-  a.flags = h->p.flags;
+  a.flags = h->p.flags & ~kFlagBaseAsync;
+  // base logits behind a slow link: copy each step's rows during the step before, where shared memory allows
+  if (base_async && pl.smem_bytes + base_in_bytes(B, pl.ng) <= h->smem_optin) a.flags |= kFlagBaseAsync;
   a.ng = pl.ng;
   a.n_smem = pl.n_smem;
   a.n_tmem = pl.n_tmem;
@@ -561,20 +518,20 @@ int whead_advance(whead_t* h, const int32_t* x, const float* s, float* s_next, i
 }
 
 namespace {
-// A pointer this GPU can read the caller's memory through, or nullptr: memory of this device, managed
+// A pointer this GPU can reach the caller's memory through, or nullptr: memory of this device, managed
 // memory, host memory pinned and mapped by CUDA, or any host memory where the GPU walks the host's page
 // tables (as on Grace over NVLink-C2C).
-const float* device_view(const whead_t* h, const float* p) {
+void* device_view(const whead_t* h, const void* p) {
   cudaPointerAttributes at{};
   if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
     (void)cudaGetLastError();
     return nullptr;
   }
   switch (at.type) {
-    case cudaMemoryTypeDevice: return at.device == h->device ? p : nullptr;
-    case cudaMemoryTypeManaged: return p;
-    case cudaMemoryTypeHost: return static_cast<const float*>(at.devicePointer);
-    default: return h->pageable_access ? p : nullptr;
+    case cudaMemoryTypeDevice: return at.device == h->device ? const_cast<void*>(p) : nullptr;
+    case cudaMemoryTypeManaged: return const_cast<void*>(p);
+    case cudaMemoryTypeHost: return at.devicePointer;
+    default: return h->pageable_access ? const_cast<void*>(p) : nullptr;
   }
 }
 }  // namespace
@@ -594,10 +551,13 @@ int whead_walk_host(whead_t* h, const float* base_host, const float* u0_host, in
     const size_t cap = (size_t)h->p.max_B * h->p.max_gamma * h->p.V;
     if (cudaMalloc(&h->d_logits, cap * logit_elem) != cudaSuccess) return WHEAD_ERR_CUDA;
   }
-  // the walk reads each step's base logits where the caller keeps them when the GPU can address that memory
-  // (the kernel asks L2 for step t + 1's rows during step t, which hides the host link's latency); otherwise
-  // they are copied to a device buffer first
-  const float* base = (h->p.flags & WHEAD_FLAG_HOST_STAGE) ? nullptr : device_view(h, base_host);
+  // The walk reads each step's base logits where the caller keeps them when the GPU can address that memory,
+  // copying step t + 1's rows into shared memory asynchronously during step t, which hides the host link's
+  // latency; it reads u0 and writes the tokens in place on the same condition. Whatever it cannot reach is
+  // copied through handle-owned device buffers.
+  const bool stage = (h->p.flags & WHEAD_FLAG_HOST_STAGE) != 0u;
+  const float* base = stage ? nullptr : static_cast<const float*>(device_view(h, base_host));
+  const bool in_place = base != nullptr;
   if (!base) {
     if (!h->d_base) {
       const size_t cap = (size_t)h->p.max_B * h->p.max_gamma * h->p.V;
@@ -607,13 +567,19 @@ int whead_walk_host(whead_t* h, const float* base_host, const float* u0_host, in
       return WHEAD_ERR_CUDA;
     base = h->d_base;
   }
-  if (cudaMemcpyAsync(h->d_u0, u0_host, (size_t)B * h->p.r * 4, cudaMemcpyDefault, h->stream) != cudaSuccess)
-    return WHEAD_ERR_CUDA;
-  const int rc = walk_impl(h, base, h->d_u0, B, gamma, T, seed, 0, h->d_tok, nullptr,
-                           out_logits_host ? h->d_logits : nullptr, nullptr);
+  const float* u0 = stage ? nullptr : static_cast<const float*>(device_view(h, u0_host));
+  if (!u0 || !aligned16(u0)) {
+    if (cudaMemcpyAsync(h->d_u0, u0_host, (size_t)B * h->p.r * 4, cudaMemcpyDefault, h->stream) != cudaSuccess)
+      return WHEAD_ERR_CUDA;
+    u0 = h->d_u0;
+  }
+  int32_t* tok = stage ? nullptr : static_cast<int32_t*>(device_view(h, out_tokens_host));
+  if (!tok) tok = h->d_tok;
+  const int rc = walk_impl(h, base, u0, B, gamma, T, seed, 0, tok, nullptr, out_logits_host ? h->d_logits : nullptr,
+                           nullptr, in_place);
   if (rc != WHEAD_OK) return rc;
-  if (cudaMemcpyAsync(out_tokens_host, h->d_tok, (size_t)B * gamma * 4, cudaMemcpyDefault, h->stream) !=
-      cudaSuccess)
+  if (tok == h->d_tok &&
+      cudaMemcpyAsync(out_tokens_host, h->d_tok, (size_t)B * gamma * 4, cudaMemcpyDefault, h->stream) != cudaSuccess)
     return WHEAD_ERR_CUDA;
   if (out_logits_host &&
       cudaMemcpyAsync(out_logits_host, h->d_logits, nbase * logit_elem, cudaMemcpyDefault, h->stream) != cudaSuccess)
@@ -730,43 +696,10 @@ int noalloc_setup(int dev, NaDevice** out) {
   return WHEAD_OK;
 }
 
-template <int KB, int NH, bool NB1>
-int noalloc_launch_t(const CUtensorMap& tmap, const CUtensorMap& tmap128, cudaStream_t stream, int smem_optin,
-                     const Plan& pl, const WalkArgs& a) {
-  auto fn = walk_kernel<KB, NH, NB1, false>;
-  if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_optin) != cudaSuccess)
-    return WHEAD_ERR_CUDA;
-  void* args[] = {(void*)&tmap, (void*)&tmap128, (void*)&a};
-  cudaError_t e = cudaLaunchCooperativeKernel((const void*)fn, dim3(pl.G), dim3(kThreads), args, (size_t)pl.smem_bytes,
-                                              stream);
-  if (e == cudaErrorCooperativeLaunchTooLarge) {
-    (void)cudaGetLastError();
-    return WHEAD_ERR_NO_COOP;
-  }
-  if (e != cudaSuccess) {
-    (void)cudaGetLastError();
-    return WHEAD_ERR_CUDA;
-  }
-  return WHEAD_OK;
-}
-
 int noalloc_launch(int r, int NH, const CUtensorMap& tmap, const CUtensorMap& tmap128, cudaStream_t stream,
                    int smem_optin, const Plan& pl, const WalkArgs& a) {
-  switch (kb_of(r) * 4 + (NH - 1) * 2 + (a.B == 1 ? 1 : 0)) {
-    case 4: return noalloc_launch_t<1, 1, false>(tmap, tmap128, stream, smem_optin, pl, a);
-    case 5: return noalloc_launch_t<1, 1, true>(tmap, tmap128, stream, smem_optin, pl, a);
-    case 6: return noalloc_launch_t<1, 2, false>(tmap, tmap128, stream, smem_optin, pl, a);
-    case 8: return noalloc_launch_t<2, 1, false>(tmap, tmap128, stream, smem_optin, pl, a);
-    case 9: return noalloc_launch_t<2, 1, true>(tmap, tmap128, stream, smem_optin, pl, a);
-    case 10: return noalloc_launch_t<2, 2, false>(tmap, tmap128, stream, smem_optin, pl, a);
-    case 12: return noalloc_launch_t<3, 1, false>(tmap, tmap128, stream, smem_optin, pl, a);
-    case 13: return noalloc_launch_t<3, 1, true>(tmap, tmap128, stream, smem_optin, pl, a);
-    case 14: return noalloc_launch_t<3, 2, false>(tmap, tmap128, stream, smem_optin, pl, a);
-    case 16: return noalloc_launch_t<4, 1, false>(tmap, tmap128, stream, smem_optin, pl, a);
-    case 17: return noalloc_launch_t<4, 1, true>(tmap, tmap128, stream, smem_optin, pl, a);
-    case 18: return noalloc_launch_t<4, 2, false>(tmap, tmap128, stream, smem_optin, pl, a);
-    default: return WHEAD_ERR_UNSUPPORTED;
-  }
+  const WalkLaunch l{&tmap, &tmap128, stream, smem_optin, pl.G, pl.smem_bytes, r, NH, false};
+  return launch_walk_resident(l, a);
 }
 
 }  // namespace

@@ -125,11 +125,12 @@ def test_host_entry_point_matches_device(torch_cuda):
     head.close()
 
 
-@pytest.mark.parametrize("memory", ["pinned", "pageable", "staged"])
+@pytest.mark.parametrize("memory", ["pinned", "pageable", "staged", "u0_unaligned"])
 def test_host_entry_point_base_in_place_or_staged(torch_cuda, memory):
-    """whead_walk_host reads the base logits where they lie when the GPU can address them (pinned memory; any
-    host memory where the GPU walks the host's page tables) and copies them first otherwise or when asked to
-    (FLAG_HOST_STAGE); tokens and logits must equal those of the walk on device buffers, call after call."""
+    """whead_walk_host reads the base logits and u0, and writes the tokens, where they lie when the GPU can
+    address them (pinned memory; any host memory where the GPU walks the host's page tables), and copies them
+    otherwise or when asked to (FLAG_HOST_STAGE; a u0 off a 16-byte boundary is copied too); tokens and logits
+    must equal those of the walk on device buffers, call after call."""
     from speculative_decoding_serial_gb300 import whead as wh
     torch = torch_cuda
     d = I.make_inputs(O.MARKOV, 20011, 256, 3, 16, seed=33)
@@ -143,6 +144,11 @@ def test_host_entry_point_base_in_place_or_staged(torch_cuda, memory):
     lg_host = torch.empty((3, 16, 20011), dtype=torch.float32)
     if memory == "pinned":
         base_h, s0_h, lg_host = base_h.pin_memory(), s0_h.pin_memory(), lg_host.pin_memory()
+    if memory == "u0_unaligned":
+        buf = torch.empty(s0_h.numel() + 1, dtype=torch.float32)
+        s0_h = buf[1:].view(s0_h.shape)  # 4 bytes past an allocation's start
+        s0_h.copy_(torch.from_numpy(d["s0"]))
+        assert s0_h.data_ptr() % 16 != 0
     for k in range(3):
         if k == 2:
             base_h = base_h.clone()  # a different buffer on the last call
