@@ -160,6 +160,41 @@ def test_host_entry_point_base_in_place_or_staged(torch_cuda, memory):
     head.close()
 
 
+HOST_VARIANTS = [
+    # kind, V, r, B, gamma, T, flags: each kernel family of the host-buffer walk (asynchronous base copies
+    # where the second buffer fits; at B = 16 it does not, and the walk reads host memory in place)
+    (O.MARKOV, 30011, 256, 1, 6, 0.0, 0),
+    (O.MARKOV, 30011, 256, 1, 6, 1.0, 0),
+    (O.MARKOV, 12000, 64, 16, 3, 1.0, 0),
+    (O.RECURRENT, 9001, 128, 1, 5, 0.0, 0),
+    (O.RECURRENT, 9001, 192, 3, 4, 1.0, 0),
+    (O.MARKOV, 20000, 256, 1, 5, 0.0, "e4m3"),
+    (O.MARKOV, 20000, 128, 4, 4, 1.0, "e4m3"),
+]
+
+
+@pytest.mark.parametrize("kind,V,r,B,gamma,T,wfmt", HOST_VARIANTS)
+def test_host_entry_point_kernel_variants(torch_cuda, kind, V, r, B, gamma, T, wfmt):
+    """Tokens, logits and the device status of whead_walk_host on pinned host buffers equal those of the walk
+    on device buffers with the same handle (bit for bit: the same arithmetic, another copy of the base logits)."""
+    from speculative_decoding_serial_gb300 import whead as wh
+    torch = torch_cuda
+    d = I.make_inputs(kind, V, r, B, gamma, seed=V + B)
+    dd = to_device(d, "cuda")
+    flags = wh.FLAG_LOGITS_F32 | (wh.FLAG_W_E4M3 if wfmt == "e4m3" else 0)
+    head = wh.Head(dd["W"], dd["E"], kind=kind, A=dd["A"], c=dd["c"], max_B=B, max_gamma=gamma, flags=flags)
+    lg_dev = torch.empty((B, gamma, V), dtype=torch.float32, device="cuda")
+    dev_tok = head.walk(dd["base"], dd["s0"], T=T, seed=11, out_logits=lg_dev).cpu()
+    lg_host = torch.empty((B, gamma, V), dtype=torch.float32).pin_memory()
+    host_tok = head.walk_host(torch.from_numpy(d["base"]).pin_memory(), torch.from_numpy(d["s0"]).pin_memory(),
+                              T=T, seed=11, out_tokens=torch.empty((B, gamma), dtype=torch.int32).pin_memory(),
+                              out_logits=lg_host)
+    assert torch.equal(dev_tok, host_tok)
+    assert torch.equal(lg_dev.cpu(), lg_host)
+    assert head.status() == 0
+    head.close()
+
+
 def test_host_entry_point_reports_device_errors(torch_cuda):
     """A walk whose bounded waits run out makes whead_walk_host return WHEAD_ERR_TIMEOUT (and clear it)."""
     from speculative_decoding_serial_gb300 import whead as wh
