@@ -61,8 +61,8 @@ typedef enum { WHEAD_MARKOV = 0, WHEAD_RECURRENT = 1 } whead_kind;
                                         handle-owned copy (whead_quantize_w_e4m3), and every step splits the state
                                         into two scaled E4M3 vectors whose projections are scaled and summed.
                                         Requires r = 128 or 256 and max_B <= 4; not with whead_walk_noalloc. */
-#define WHEAD_FLAG_HOST_STAGE (1u << 5)  /* whead_walk_host copies the base logits to a device buffer before the walk
-                                           even where the GPU could read the caller's memory in place */
+#define WHEAD_FLAG_HOST_STAGE (1u << 5)  /* whead_walk_host copies base logits and u0 in and the tokens out through
+                                           device buffers even where the GPU could reach the caller's memory */
 #define WHEAD_FLAG_FAULT_SKIP_ARRIVAL (1u << 8) /* testing: CTA 0 never arrives at step 0's exchange, so
                                                    every other CTA's bounded wait runs out */
 
