@@ -218,13 +218,13 @@ int whead_destroy(whead_t* h);
  * scratch would exceed WHEAD_NOALLOC_SCRATCH_BYTES is rejected with WHEAD_ERR_UNSUPPORTED: more than 16
  * walks, more than 64 steps, or a grid of more than 256 CTAs (more SMs than this array has slots for).
  *
- * Every call shares the one array and clears what must start at zero (exchange slots, counter, status)
- * with cudaMemsetAsync on the call's stream. Calls whose walks overlap on the GPU (different streams, or several
+ * Every call shares the one array and clears what must start at zero (exchange slots, counter, status and,
+ * for the recurrent head, the tagged A h slices) with cudaMemsetAsync on the call's stream. Calls whose walks overlap on the GPU (different streams, or several
  * host threads) race on the array and give wrong results: serialize them. The first call on a device
  * looks up the array's device address (cudaGetSymbolAddress) and the device's limits; make that first call
  * before any stream capture.
  */
-#define WHEAD_NOALLOC_SCRATCH_BYTES (128 * 1024)
+#define WHEAD_NOALLOC_SCRATCH_BYTES (192 * 1024)
 int whead_walk_noalloc(const void* W, const void* E, const whead_params* params, const float* base,
                        const float* u0, int32_t B, int32_t gamma, float T, uint64_t seed, int32_t* out_tokens,
                        void* out_logits, int32_t* out_status);

@@ -75,7 +75,10 @@ struct WalkArgs {
   unsigned long long* slots_reset;  // the other call parity (or null): cleared during this call
   unsigned int* cnt_reset;
   int32_t slots_reset_count;        // words to clear at slots_reset
-  float* ah;                        // [2][kMaxB][r]: slices of A h exchanged between CTAs
+  unsigned long long* ah;           // [2 step parities][B][r]: slices of A h exchanged between CTAs, each word
+                                    // (t + 1) << 32 | fp32 bits, written relaxed and read until the tag is step t's
+  unsigned long long* ah_reset;     // the other call parity's slices (or null): cleared during this call
+  int32_t ah_reset_count;           // words to clear at ah_reset
   int* status;
   unsigned long long* trace;  // optional phase stamps: [grid][trace_stride] (clock64 half, globaltimer half)
   int32_t trace_stride;
@@ -706,6 +709,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = tid; i < P.slots_reset_count; i += kThreads) P.slots_reset[i] = 0ull;
     if (tid == 0) *P.cnt_reset = 0u;
   }
+  if (cta == G - 1 && P.ah_reset != nullptr)
+    for (int i = tid; i < P.ah_reset_count; i += kThreads) P.ah_reset[i] = 0ull;
   tmem_fence_before();
   __syncthreads();
   tmem_fence_after();
@@ -896,7 +901,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = lane; k < r; k += 32) s = fmaf(s_A[i * r + k], s_h[n * r + k], s);
 #pragma unroll
           for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-          if (lane == 0) P.ah[((int64_t)(t & 1) * kMaxB + n) * r + a_lo + i] = s;
+          if (lane == 0) {
+            const unsigned long long word = ((unsigned long long)(t + 1) << 32) | __float_as_uint(s);
+            asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(P.ah + ((int64_t)(t & 1) * B + n) * r + a_lo + i),
+                         "l"(word)
+                         : "memory");
+          }
         }
       }
 
@@ -1294,13 +1304,31 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       } else {
-        const float* ah = P.ah + (int64_t)(t & 1) * kMaxB * r;
+        // the slices carry step t's tag once their stores are visible (every CTA wrote its slice before it
+        // arrived, so the wait is short); running out of time sets the time-out status and ends the walk
+        const unsigned long long* ah = P.ah + (int64_t)(t & 1) * B * r;
+        const uint64_t t_wait = globaltimer_ns();
+        bool ah_late = false;
         for (int i = tid; i < B * r; i += kThreads) {
           const int n = i / r, k = i % r;
           const float e = __uint_as_float((uint32_t)P.E[(int64_t)s_win[n] * r + k] << 16);
-          float pre = __fadd_rn(__ldcg(ah + n * r + k), e);
+          unsigned long long word = 0ull;
+          for (uint32_t spins = 0;; ++spins) {
+            asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(word) : "l"(ah + i) : "memory");
+            if ((uint32_t)(word >> 32) == (uint32_t)(t + 1)) break;
+            if ((spins & 15u) == 15u && globaltimer_ns() - t_wait > P.timeout_ns) {
+              ah_late = true;
+              break;
+            }
+          }
+          if (ah_late) break;
+          float pre = __fadd_rn(__uint_as_float((uint32_t)word), e);
           if (P.c) pre = __fadd_rn(pre, P.c[k]);
           s_h[i] = tanhf(pre);
+        }
+        if (ah_late) {
+          atomicCAS(P.status, 0, kStatusTimeout);
+          *s_abort = 1;
         }
         __syncthreads();
         if constexpr (F8) {

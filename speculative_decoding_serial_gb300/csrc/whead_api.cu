@@ -32,7 +32,7 @@ struct Plan {
 struct Scratch {
   unsigned long long* slots;  // [2 call parities][2 step parities][sm_count][kMaxB]
   unsigned int* cnt;          // two counters, 128 bytes apart
-  float* ah;                  // [2][kMaxB][r]
+  unsigned long long* ah;     // [2 call parities][2 step parities][kMaxB][r] tagged words
   int* status;
 };
 
@@ -208,6 +208,9 @@ int launch(whead_t* h, const Plan& pl, const WalkArgs& a, int NH) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Tagged A h words of one call parity: two step parities of up to kMaxB walks.
+size_t ah_words_per_parity(int r) { return 2 * (size_t)kMaxB * r; }
 
 // The next state of B walks for given winners x (global rows of E), one warp per (walk, element): Markov
 // s_next[b] = E[x_b] (bf16 to fp32); recurrent s_next[b][i] = tanh(A[i,:] . s[b] + E[x_b, i] + c[i]) with the
@@ -401,17 +404,18 @@ int whead_create(const void* W, const void* E, const whead_params* params, whead
   if (encode_w(&h->tmap, Wt, p.V, rw, kGroupRows) != WHEAD_OK) return fail(WHEAD_ERR_CUDA);
   if (encode_w(&h->tmap128, Wt, p.V, rw, kGroupRows * kTmaChunkGroups) != WHEAD_OK) return fail(WHEAD_ERR_CUDA);
 
-  // scratch: exchange slots (two call parities), two counters on their own lines, A h slices, status word
+  // scratch: exchange slots (two call parities), two counters on their own lines, A h slices (two call
+  // parities), status word
   const size_t slots_bytes = 2 * (size_t)h->slots_per_parity * 8;
   const size_t cnt_bytes = 256;
-  const size_t ah_bytes = 2 * (size_t)kMaxB * p.r * 4;
+  const size_t ah_bytes = 2 * ah_words_per_parity(p.r) * 8;
   const size_t total = slots_bytes + cnt_bytes + ah_bytes + 256;
   if (cudaMalloc(&h->scratch_block, total) != cudaSuccess) return fail(WHEAD_ERR_CUDA);
   if (cudaMemset(h->scratch_block, 0, total) != cudaSuccess) return fail(WHEAD_ERR_CUDA);
   uint8_t* b = static_cast<uint8_t*>(h->scratch_block);
   h->s.slots = reinterpret_cast<unsigned long long*>(b);
   h->s.cnt = reinterpret_cast<unsigned int*>(b + slots_bytes);
-  h->s.ah = reinterpret_cast<float*>(b + slots_bytes + cnt_bytes);
+  h->s.ah = reinterpret_cast<unsigned long long*>(b + slots_bytes + cnt_bytes);
   h->s.status = reinterpret_cast<int*>(b + slots_bytes + cnt_bytes + ah_bytes);
   *out = h;
   return WHEAD_OK;
@@ -461,7 +465,9 @@ int walk_impl(whead_t* h, const float* base, const float* s0, int32_t B, int32_t
   a.slots_reset = h->s.slots + (size_t)(par ^ 1u) * h->slots_per_parity;
   a.slots_reset_count = (int32_t)h->slots_per_parity;
   a.cnt_reset = h->s.cnt + (par ^ 1u) * 32;
-  a.ah = h->s.ah;
+  a.ah = h->s.ah + (size_t)par * ah_words_per_parity(h->p.r);
+  a.ah_reset = h->s.ah + (size_t)(par ^ 1u) * ah_words_per_parity(h->p.r);
+  a.ah_reset_count = (int32_t)ah_words_per_parity(h->p.r);
   a.status = h->s.status;
   if (h->trace && h->trace_bytes >= (int64_t)pl.G * trace_stride_for(gamma) * 8) {
     a.trace = h->trace;
@@ -657,13 +663,14 @@ int whead_destroy(whead_t* h) {
 namespace {
 
 // Layout of the array: [slots: 2 step parities x up to 256 CTAs x 16 walks, 64 KB][counter 128 B][status 128 B]
-// [A h slices 32 KB]. Slots, counter and status are cleared by the host before every call.
+// [tagged A h slices: 2 step parities x B x r words, up to 64 KB]. Slots, counter, status and the slices of
+// the call are cleared by the host before every call.
 constexpr int kNaMaxGrid = kMaxGrid;
 constexpr size_t kNaSlots = 2 * (size_t)kNaMaxGrid * kMaxB * 8;
 constexpr size_t kNaCntOff = kNaSlots;
 constexpr size_t kNaStatusOff = kNaCntOff + 128;
 constexpr size_t kNaAhOff = kNaStatusOff + 128;
-static_assert(kNaAhOff + 2 * (size_t)kMaxB * 256 * 4 <= WHEAD_NOALLOC_SCRATCH_BYTES, "scratch array too small");
+static_assert(kNaAhOff + 2 * (size_t)kMaxB * 256 * 8 <= WHEAD_NOALLOC_SCRATCH_BYTES, "scratch array too small");
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[WHEAD_NOALLOC_SCRATCH_BYTES];
 
@@ -720,7 +727,7 @@ extern "C" int whead_walk_noalloc(const void* W, const void* E, const whead_para
   if (p.v_offset + p.V >= (int64_t)1 << 24) return WHEAD_ERR_UNSUPPORTED;
   if (!(T >= 0.0f) || T > 3.0e38f) return WHEAD_ERR_INVALID_ARG;
   if (!aligned16(W) || !aligned16(E) || !aligned16(u0)) return WHEAD_ERR_INVALID_ARG;
-  const size_t need = kNaAhOff + 2 * (size_t)kMaxB * p.r * 4;
+  const size_t need = kNaAhOff + 2 * (size_t)B * p.r * 8;
   if (need > WHEAD_NOALLOC_SCRATCH_BYTES) return WHEAD_ERR_UNSUPPORTED;
 
   int dev = 0;
@@ -743,6 +750,8 @@ extern "C" int whead_walk_noalloc(const void* W, const void* E, const whead_para
   uint8_t* sc = static_cast<uint8_t*>(nd->scratch);
   if (cudaMemsetAsync(sc, 0, 2 * (size_t)pl.G * B * 8, stream) != cudaSuccess) return WHEAD_ERR_CUDA;
   if (cudaMemsetAsync(sc + kNaCntOff, 0, 256, stream) != cudaSuccess) return WHEAD_ERR_CUDA;
+  if (p.kind == WHEAD_RECURRENT && cudaMemsetAsync(sc + kNaAhOff, 0, 2 * (size_t)B * p.r * 8, stream) != cudaSuccess)
+    return WHEAD_ERR_CUDA;
   if (out_status && cudaMemsetAsync(out_status, 0, sizeof(int32_t), stream) != cudaSuccess) return WHEAD_ERR_CUDA;
 
   WalkArgs a;
@@ -762,7 +771,8 @@ extern "C" int whead_walk_noalloc(const void* W, const void* E, const whead_para
   a.cnt = reinterpret_cast<unsigned int*>(sc + kNaCntOff);
   a.slots_reset = nullptr;  // cleared above by the host
   a.cnt_reset = nullptr;
-  a.ah = reinterpret_cast<float*>(sc + kNaAhOff);
+  a.ah = reinterpret_cast<unsigned long long*>(sc + kNaAhOff);
+  a.ah_reset = nullptr;  // cleared above by the host
   a.status = out_status ? reinterpret_cast<int*>(out_status) : reinterpret_cast<int*>(sc + kNaStatusOff);
   a.V = p.V;
   a.v_offset = p.v_offset;
