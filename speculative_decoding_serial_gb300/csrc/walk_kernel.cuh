@@ -599,13 +599,63 @@ __device__ __forceinline__ void stage_base(const WalkArgs& P, float* s_base, int
   const int i0 = (int)threadIdx.x - first;
   if (i0 < 0 || i0 >= count || t >= P.gamma) return;
   const int valid = (int)min((int64_t)rows, P.V - row_base);  // rows of this CTA below V (may be <= 0)
-  for (int n = 0; n < P.B; ++n) {
-    const float* src = P.base + ((int64_t)n * P.gamma + t) * P.V + row_base;
-    float* dst = s_base + n * rows;
-    for (int lr = i0; lr < rows; lr += count) dst[lr] = (lr < valid) ? __ldg(src + lr) : 0.f;
-    if (t + 1 < P.gamma)
-      for (int lr = 32 * i0; lr < valid; lr += 32 * count) prefetch_l2(src + P.V + lr);
+  // (walk, row) pairs flattened; each thread issues four loads before it stores any of them, so their
+  // latencies overlap instead of adding up
+  const int total = P.B * rows;
+  for (int i = i0; i < total; i += 4 * count) {
+    float x[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int k = i + u * count, n = k / rows, lr = k - n * rows;
+      x[u] = (k < total && lr < valid) ? __ldg(P.base + ((int64_t)n * P.gamma + t) * P.V + row_base + lr) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (i + u * count < total) s_base[i + u * count] = x[u];
   }
+  if (t + 1 < P.gamma)
+    for (int n = 0; n < P.B; ++n) {
+      const float* nxt = P.base + ((int64_t)n * P.gamma + t + 1) * P.V + row_base;
+      for (int lr = 32 * i0; lr < valid; lr += 32 * count) prefetch_l2(nxt + lr);
+    }
+}
+
+// The same rows as stage_base, copied with cp.async so that no thread waits for them here: 16 bytes per copy
+// when every row of base starts on a 16-byte boundary (rows past V zero-filled by the copy's source size), else
+// 4 bytes per copy. The caller runs cp.async.wait_all before the rows are read. Also asks L2 for step t + 1.
+__device__ __forceinline__ void stage_base_cp(const WalkArgs& P, float* s_base, int64_t row_base, int t, int first,
+                                              int count) {
+  const int rows = P.ng * kGroupRows;
+  const int i0 = (int)threadIdx.x - first;
+  if (i0 < 0 || i0 >= count || t >= P.gamma) return;
+  const int valid = (int)min((int64_t)rows, P.V - row_base);  // rows of this CTA below V (may be <= 0)
+  if ((P.V & 3) == 0 && (reinterpret_cast<uintptr_t>(P.base) & 15u) == 0) {
+    const int chunks = rows / 4;  // rows is a multiple of 16
+    for (int i = i0; i < P.B * chunks; i += count) {
+      const int n = i / chunks, lr = 4 * (i - n * chunks);
+      const int nbytes = 4 * max(0, min(4, valid - lr));
+      // a copy with no source bytes still names an address inside base
+      const float* src = nbytes ? P.base + ((int64_t)n * P.gamma + t) * P.V + row_base + lr : P.base;
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(s_base + n * rows + lr)), "l"(src),
+                   "r"(nbytes)
+                   : "memory");
+    }
+  } else {
+    for (int i = i0; i < P.B * rows; i += count) {
+      const int n = i / rows, lr = i - n * rows;
+      if (lr < valid)
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(s_base + i)),
+                     "l"(P.base + ((int64_t)n * P.gamma + t) * P.V + row_base + lr)
+                     : "memory");
+      else
+        s_base[i] = 0.f;
+    }
+  }
+  if (t + 1 < P.gamma)
+    for (int n = 0; n < P.B; ++n) {
+      const float* nxt = P.base + ((int64_t)n * P.gamma + t + 1) * P.V + row_base;
+      for (int lr = 32 * i0; lr < valid; lr += 32 * count) prefetch_l2(nxt + lr);
+    }
 }
 
 // The same rows as stage_base, copied asynchronously into a second buffer (cp.async, 4 bytes per row; the
@@ -639,6 +689,39 @@ __device__ __forceinline__ void move_base(const WalkArgs& P, float* s_base, cons
   if (i0 < 0 || i0 >= count || t >= P.gamma) return;
   for (int n = 0; n < P.B; ++n)
     for (int lr = i0; lr < rows; lr += count) s_base[n * rows + lr] = s_in[n * rows + lr];
+}
+
+// Several walks: one warp reads every CTA's slot of walk n until each word carries step t's tag (re-reading the
+// stale ones; bounded by timeout_ns from t_start) and returns the largest packed key in every lane, or 0 on
+// time-out. The warp takes its decision on leaving the loop as a whole.
+template <int kSlotsPerLane>
+__device__ __forceinline__ unsigned long long read_walk_slots(const unsigned long long* sl, int G, int B, int n, int t,
+                                                              int lane, uint64_t t_start, uint64_t timeout_ns,
+                                                              bool& late) {
+  const unsigned long long tag = (unsigned long long)(t + 1) << 56;
+  unsigned long long w[kSlotsPerLane];
+#pragma unroll
+  for (int i = 0; i < kSlotsPerLane; ++i) w[i] = (lane + 32 * i < G) ? 0ull : tag;  // tag 0: not read yet
+  for (uint32_t spins = 0;; ) {
+#pragma unroll
+    for (int i = 0; i < kSlotsPerLane; ++i) {
+      const int cc = lane + 32 * i;
+      if (cc < G && (w[i] >> 56) != (unsigned long long)(t + 1))
+        asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w[i]) : "l"(sl + (int64_t)cc * B + n) : "memory");
+    }
+    bool fresh = true;
+#pragma unroll
+    for (int i = 0; i < kSlotsPerLane; ++i) fresh = fresh && ((w[i] >> 56) == (unsigned long long)(t + 1));
+    if (__all_sync(0xffffffffu, fresh)) break;
+    if ((++spins & 15u) == 0u && __any_sync(0xffffffffu, globaltimer_ns() - t_start > timeout_ns)) {
+      late = true;
+      return 0ull;
+    }
+  }
+  unsigned long long best = 0ull;
+#pragma unroll
+  for (int i = 0; i < kSlotsPerLane; ++i) best = umax64(best, w[i] & 0x00FFFFFFFFFFFFFFull);
+  return warp_max64((uint32_t)(best >> 32), (uint32_t)best);
 }
 
 // ------------------------------------------------------------------------------------------------
@@ -681,6 +764,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* s_q = smem + L.q;                            // E4M3 weights: each walk's state as two E4M3 vectors
   float* s_qs = reinterpret_cast<float*>(smem + L.qs);  // and their scales
   static_assert(!F8 || NH == 1, "E4M3 weights take two accumulator columns per walk: at most 4 walks");
+  // several walks with bf16 W: the warps read the walks' exchange slots in parallel (E4M3 weights keep the serial
+  // reads, which let the exchange warp split the winners' E rows before the barrier)
+  constexpr bool kParRead = !NB1 && !F8;
 
   const uint32_t mbar = smem_u32(s_mbar);
   trace_stamp(P, 0);
@@ -769,6 +855,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+  // register-resident group of a register warp: its loads are issued here, so they land while the rest of the
+  // entry runs (register warps own no tensor-memory group)
+  uint32_t rfA[KB][16];
+  if (NH == 1 && rf_warp) {  // the planner gives register groups only to batches of up to 8 walks
+    int jr = -1;
+    for (int e = 0; e < my_count; ++e) {
+      const uint32_t ent = __shfl_sync(0xffffffffu, my_entry, e);
+      if (((ent >> 8) & 3u) == kTierRf) jr = (int)(ent & 0xFFu);
+    }
+#pragma unroll
+    for (int bx = 0; bx < KB; ++bx) {
+      if (jr >= 0) {
+        uint32_t a[16];
+        load_box_global(a, P.W, row_base + (int64_t)kGroupRows * jr + g, V, P.rw, bx, c);
+        rows_to_fragments(rfA[bx], a);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) rfA[bx][i] = 0u;
+      }
+    }
+  }
   // streamed groups: ask L2 for their rows now, so that every step reads them from L2
   for (int e = 0; e < my_count; ++e) {
     const uint32_t ent = __shfl_sync(0xffffffffu, my_entry, e);
@@ -845,26 +952,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------- the walk ----------------
   auto walk = [&](auto rf_tag) {
     constexpr bool RFW = decltype(rf_tag)::value;
-    // register-resident group of this warp (RF warps only)
-    uint32_t rfA[RFW ? KB : 1][16];
-    if constexpr (RFW) {
-      int jr = -1;
-      for (int e = 0; e < my_count; ++e) {
-        const uint32_t ent = __shfl_sync(0xffffffffu, my_entry, e);
-        if (((ent >> 8) & 3u) == kTierRf) jr = (int)(ent & 0xFFu);
-      }
-#pragma unroll
-      for (int bx = 0; bx < KB; ++bx) {
-        if (jr >= 0) {
-          uint32_t a[16];
-          load_box_global(a, P.W, row_base + (int64_t)kGroupRows * jr + g, V, P.rw, bx, c);
-          rows_to_fragments(rfA[bx], a);
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) rfA[bx][i] = 0u;
-        }
-      }
-    }
 
     uint32_t bf[NH][KB][kBfWords<F8>];
     // E4M3 weights: the scales of walk c's two state vectors (this lane's accumulator columns 2c, 2c + 1)
@@ -1144,8 +1231,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           move_base(P, s_base, s_base_in, t + 1, 32, kThreads - 32);
           copy_base_async(P, s_base_in, row_base, t + 2, 32, kThreads - 32);
         }
-      } else {
+      } else if constexpr (NB1) {
         stage_base(P, s_base, row_base, t + 1, 32, kThreads - 32);
+      } else {
+        // several walks: a few rows per walk and thread, so the copies run asynchronously (measured faster than
+        // register loads from B = 2 up; slower for one walk)
+        stage_base_cp(P, s_base, row_base, t + 1, 32, kThreads - 32);
       }
 
       // exchange (Fig. 8). Each CTA publishes its winner for walk n as one 64-bit word in its own slot,
@@ -1191,7 +1282,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         const unsigned int target = (unsigned int)(t + 1) * (unsigned int)G;
         const unsigned int near = target - (unsigned int)min(G, 4);
         bool late = false;
-        for (int n = 0; n < B && !late; ++n) {
+        if constexpr (kParRead) {
+          // several walks: this warp waits only until all but a few CTAs have arrived; after the barrier below
+          // the warps read the slots of their walks side by side
+          for (uint32_t spins = 0;; ) {
+            unsigned int now = 0;
+            if (lane == 0) asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(now) : "l"(P.cnt) : "memory");
+            if (__shfl_sync(0xffffffffu, now, 0) >= near) break;
+            if ((++spins & 15u) == 0u && __any_sync(0xffffffffu, globaltimer_ns() - t_start > P.timeout_ns)) {
+              late = true;
+              break;
+            }
+          }
+        }
+        for (int n = 0; n < B && !late && !kParRead; ++n) {
           unsigned long long w[kSlotsPerLane];
 #pragma unroll
           for (int i = 0; i < kSlotsPerLane; ++i) w[i] = (lane + 32 * i < G) ? 0ull : tag;  // tag 0: not read yet
@@ -1270,8 +1374,42 @@ __global__ void __launch_bounds__(kThreads, 1)
             });
           }
         }
+        if constexpr (!kParRead) trace_stamp(P, 2 + kTraceStampsPerStep * t + 2);
+      }
+      if constexpr (kParRead) {
+        // several walks, bf16 W: every warp that keeps no register group reads the slots of walks k, k + m, ...
+        // (k its rank among those m warps), so the walks' reads overlap instead of following one another
+        __syncthreads();
+        if constexpr (!RFW) {
+          if (!*s_abort) {
+            const uint32_t others = ~P.rf_warp_mask & ((1u << kWarps) - 1u);
+            const int m = __popc(others), k = __popc(others & ((1u << warp) - 1u));
+            const unsigned long long* sl = P.slots + (int64_t)(t & 1) * G * B;
+            const uint64_t t_w = globaltimer_ns();
+            bool late = false;
+            for (int n = k; n < B; n += m) {
+              const unsigned long long wk = read_walk_slots<kMaxGrid / 32>(sl, G, B, n, t, lane, t_w, P.timeout_ns, late);
+              if (late) break;
+              if (lane == 0) {
+                const int32_t x = (int32_t)(0xFFFFFFu - ((uint32_t)wk & 0xFFFFFFu));
+                s_win[n] = x;
+                if (cta == 0) {
+                  P.tokens[(int64_t)n * gamma + t] = x;
+                  if (P.keys)
+                    P.keys[(int64_t)n * gamma + t] = ((wk >> 24) << 32) | (unsigned long long)(0xFFFFFFFFu - (uint32_t)x);
+                }
+              }
+            }
+            if (late && lane == 0) {
+              atomicCAS(P.status, 0, kStatusTimeout);
+              *s_abort = 1;
+            }
+          }
+        }
         trace_stamp(P, 2 + kTraceStampsPerStep * t + 2);
       }
+      // the next step's base logits have landed in shared memory before the barrier
+      if constexpr (!base_async && !NB1) asm volatile("cp.async.wait_all;" ::: "memory");
       __syncthreads();
       if (*s_abort) break;
 
@@ -1363,7 +1501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---------------- exit ----------------
   // copies still in flight after a timed-out wait must land before the CTA's shared memory is released
   if (!tma_done) (void)mbar_wait_bounded(mbar, 0u, P.timeout_ns);
-  if constexpr (base_async) asm volatile("cp.async.wait_all;" ::: "memory");
+  asm volatile("cp.async.wait_all;" ::: "memory");
   tmem_fence_before();
   __syncthreads();
   tmem_fence_after();

@@ -210,18 +210,20 @@ def test_host_entry_point_reports_device_errors(torch_cuda):
     bad.close()
 
 
-def test_wait_limit_reports_timeout_and_context_survives(torch_cuda):
-    """CTA 0 skips its first arrival (a host flag); every other CTA's bounded wait must run out."""
+@pytest.mark.parametrize("B", [1, 4, 12])
+def test_wait_limit_reports_timeout_and_context_survives(torch_cuda, B):
+    """CTA 0 skips its first arrival (a host flag); every other CTA's bounded wait must run out. One walk waits in
+    the exchange warp alone; several walks also wait in the warps that read each walk's slots."""
     from speculative_decoding_serial_gb300 import whead as wh
-    d = I.make_inputs(O.MARKOV, 40000, 128, 1, 3, seed=2)
+    d = I.make_inputs(O.MARKOV, 40000, 128, B, 3, seed=2)
     dd = to_device(d, "cuda")
-    bad = wh.Head(dd["W"], dd["E"], kind=O.MARKOV, max_B=1, max_gamma=3, flags=wh.FLAG_FAULT_SKIP_ARRIVAL,
+    bad = wh.Head(dd["W"], dd["E"], kind=O.MARKOV, max_B=B, max_gamma=3, flags=wh.FLAG_FAULT_SKIP_ARRIVAL,
                   timeout_us=20000)
     bad.walk(dd["base"], dd["s0"])
     assert bad.status() == wh.ERR_TIMEOUT
     assert bad.status() == 0  # cleared after reading
     bad.close()
-    good = wh.Head(dd["W"], dd["E"], kind=O.MARKOV, max_B=1, max_gamma=3)
+    good = wh.Head(dd["W"], dd["E"], kind=O.MARKOV, max_B=B, max_gamma=3)
     tok = good.walk(dd["base"], dd["s0"]).cpu().numpy()
     assert good.status() == 0
     ref = O.walk(O.MARKOV, d["W"], d["E"], d["base"], d["s0"])
