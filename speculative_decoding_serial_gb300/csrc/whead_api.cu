@@ -784,7 +784,7 @@ extern "C" int whead_walk_noalloc(const void* W, const void* E, const whead_para
   a.B = B;
   a.gamma = gamma;
   a.kind = p.kind;
-  a.flags = p.flags;
+  a.flags = p.flags & ~kFlagBaseAsync;  // the library-internal launch bit is never the caller's
   a.ng = pl.ng;
   a.n_smem = pl.n_smem;
   a.n_tmem = pl.n_tmem;

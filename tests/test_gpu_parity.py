@@ -43,6 +43,11 @@ SMALL = [
     (O.MARKOV, 7777, 128, 16, 2, 0.0, 0),
     (O.MARKOV, 3001, 64, 4, 5, 1.0, 0),
     (O.MARKOV, 9000, 256, 2, 4, 0.7, 0),
+    # one sampled walk (the single-walk selection scan draws four rows' noise per Philox call)
+    (O.MARKOV, 5003, 128, 1, 5, 1.0, 0),
+    (O.MARKOV, 20011, 256, 1, 6, 0.7, 0),
+    (O.MARKOV, 30000, 64, 1, 4, 1.0, 152),
+    (O.RECURRENT, 3001, 64, 1, 4, 1.0, 0),
     (O.RECURRENT, 3001, 64, 1, 5, 0.0, 0),
     (O.RECURRENT, 9000, 256, 2, 4, 0.0, 0),
     (O.RECURRENT, 4000, 128, 3, 4, 1.0, 0),
@@ -85,14 +90,15 @@ def test_bf16_logits_single_rounding(torch_cuda):
     head.close()
 
 
-def test_resume_from_any_step_bit_exact(torch_cuda):
+@pytest.mark.parametrize("kind,B", [(O.RECURRENT, 2), (O.MARKOV, 1)])
+def test_resume_from_any_step_bit_exact(torch_cuda, kind, B):
     torch = torch_cuda
-    d = I.make_inputs(O.RECURRENT, 8000, 128, 2, 6, seed=9)
+    d = I.make_inputs(kind, 8000, 128, B, 6, seed=9)
     dd = to_device(d, "cuda")
-    head = make_head(torch_cuda, d, dd, max_B=2, max_gamma=6)
-    full = run_gpu(head, dd, 2, 6, 1.0, 77)
+    head = make_head(torch_cuda, d, dd, max_B=B, max_gamma=6)
+    full = run_gpu(head, dd, B, 6, 1.0, 77)
     for t0 in range(1, 6):
-        part = run_gpu(head, dd, 2, 6 - t0, 1.0, 77, t0=t0, base=dd["base"][:, t0:].contiguous(),
+        part = run_gpu(head, dd, B, 6 - t0, 1.0, 77, t0=t0, base=dd["base"][:, t0:].contiguous(),
                        s0=torch.from_numpy(full["state"][:, t0 - 1].copy()).cuda())
         np.testing.assert_array_equal(part["tokens"], full["tokens"][:, t0:])
         np.testing.assert_array_equal(part["z"], full["z"][:, t0:])
