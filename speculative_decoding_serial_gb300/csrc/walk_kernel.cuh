@@ -764,9 +764,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* s_q = smem + L.q;                            // E4M3 weights: each walk's state as two E4M3 vectors
   float* s_qs = reinterpret_cast<float*>(smem + L.qs);  // and their scales
   static_assert(!F8 || NH == 1, "E4M3 weights take two accumulator columns per walk: at most 4 walks");
-  // several walks with bf16 W: the warps read the walks' exchange slots in parallel (E4M3 weights keep the serial
-  // reads, which let the exchange warp split the winners' E rows before the barrier)
-  constexpr bool kParRead = !NB1 && !F8;
+  // several walks: the warps read the walks' exchange slots in parallel
+  constexpr bool kParRead = !NB1;
 
   const uint32_t mbar = smem_u32(s_mbar);
   trace_stamp(P, 0);
@@ -972,6 +971,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
     }
+
+    // E4M3 weights, Markov: warp 0 splits each winner's E row into two E4M3 vectors in shared memory
+    auto split_winner_rows = [&]() {
+      split_state_smem<KB>(s_q, s_qs, B, r, lane, [&](int w, auto& x) {
+        const int32_t xw = s_win[w];
+        uint32_t u[2 * KB];
+#pragma unroll
+        for (int e = 0; e < 2 * KB; ++e) u[e] = 0u;
+        if ((int64_t)xw >= P.v_offset && (int64_t)xw < P.v_offset + V) {
+          const uint16_t* er = P.E + (int64_t)xw * r + lane * 4 * KB;
+          if constexpr (KB == 2) {
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(er));
+            u[0] = v.x; u[1] = v.y; u[2] = v.z; u[3] = v.w;
+          } else {
+            const uint2 v = __ldg(reinterpret_cast<const uint2*>(er));
+            u[0] = v.x; u[1] = v.y;
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 2 * KB; ++e) {
+          x[2 * e] = __uint_as_float(u[e] << 16);
+          x[2 * e + 1] = __uint_as_float(u[e] & 0xFFFF0000u);
+        }
+      });
+    };
 
     for (int t = 0; t < gamma; ++t) {
       if (*s_abort) break;
@@ -1346,38 +1370,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           atomicCAS(P.status, 0, kStatusTimeout);
           *s_abort = 1;
         }
-        // E4M3 weights, Markov: the winners' E rows, split into two E4M3 vectors each, for every warp's next
+        // E4M3 weights, Markov, one walk: the winner's E row, split into two E4M3 vectors, for every warp's next
         // B fragments (a winner outside W is skipped here; the check after the barrier ends the walk)
-        if constexpr (F8) {
+        if constexpr (F8 && !kParRead) {
           if (!late && !recurrent && !(P.flags & kFlagFixedLatent)) {
             __syncwarp();
-            split_state_smem<KB>(s_q, s_qs, B, r, lane, [&](int w, auto& x) {
-              const int32_t xw = s_win[w];
-              uint32_t u[2 * KB];
-#pragma unroll
-              for (int e = 0; e < 2 * KB; ++e) u[e] = 0u;
-              if ((int64_t)xw >= P.v_offset && (int64_t)xw < P.v_offset + V) {
-                const uint16_t* er = P.E + (int64_t)xw * r + lane * 4 * KB;
-                if constexpr (KB == 2) {
-                  const uint4 v = __ldg(reinterpret_cast<const uint4*>(er));
-                  u[0] = v.x; u[1] = v.y; u[2] = v.z; u[3] = v.w;
-                } else {
-                  const uint2 v = __ldg(reinterpret_cast<const uint2*>(er));
-                  u[0] = v.x; u[1] = v.y;
-                }
-              }
-#pragma unroll
-              for (int e = 0; e < 2 * KB; ++e) {
-                x[2 * e] = __uint_as_float(u[e] << 16);
-                x[2 * e + 1] = __uint_as_float(u[e] & 0xFFFF0000u);
-              }
-            });
+            split_winner_rows();
           }
         }
         if constexpr (!kParRead) trace_stamp(P, 2 + kTraceStampsPerStep * t + 2);
       }
       if constexpr (kParRead) {
-        // several walks, bf16 W: every warp that keeps no register group reads the slots of walks k, k + m, ...
+        // several walks: every warp that keeps no register group reads the slots of walks k, k + m, ...
         // (k its rank among those m warps), so the walks' reads overlap instead of following one another
         __syncthreads();
         if constexpr (!RFW) {
@@ -1425,7 +1429,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (P.flags & kFlagFixedLatent) continue;
       if (!recurrent) {
         if constexpr (F8) {
-          // the winners' E rows were split into shared memory by the exchange warp
+          if constexpr (kParRead) {
+            // several walks: the winners are known only after the barrier, so warp 0 splits their E rows now
+            if constexpr (!RFW) {
+              if (warp == 0) split_winner_rows();
+            }
+            __syncthreads();
+          }
+          // the winners' E rows are split in shared memory
           bfrag_from_split_smem<KB>(bf, es1, es2, s_q, s_qs, B, r, lane);
         } else {
 #pragma unroll
