@@ -103,6 +103,7 @@ struct WalkArgs {
   int32_t smem_w_bytes;
   int32_t ra;        // recurrent: rows of A per CTA
   uint32_t rf_warp_mask;  // warps that keep one group in registers (they own no tensor-memory group)
+  int32_t ah_warp;        // recurrent: the warp (never a register warp) that computes the CTA's slice of A h
   int32_t wl_count[kWarps];
   // work list of each warp: bits 0..7 CTA-local group, bits 8..9 tier, bits 16..25 tensor-memory column
   uint32_t wl[kWarps][kMaxWarpGroups];
@@ -1002,14 +1003,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tau = (uint32_t)(P.t0 + t);
       trace_stamp(P, 2 + kTraceStampsPerStep * t);
 
-      // recurrent: this CTA's slice of A h_t, published with the step's arrival (warp 0, never a register warp,
-      // so the register warps' copy of the loop does not carry this code)
-      if (!RFW && recurrent && warp == 0) {
+      // recurrent: this CTA's slice of A h_t, published during the step by the least-loaded warp that keeps no
+      // register group (so the register warps' copy of the loop does not carry this code)
+      if (!RFW && recurrent && warp == P.ah_warp) {
         for (int p = 0; p < B * P.ra; ++p) {
           const int n = p / P.ra, i = p % P.ra;
           if (a_lo + i >= r) continue;
+          // r = kRank is known at compile time: the loads of a row all issue before its chain of fma
+          constexpr int kRank = (F8 ? 128 : 64) * KB;
           float s = 0.f;
-          for (int k = lane; k < r; k += 32) s = fmaf(s_A[i * r + k], s_h[n * r + k], s);
+#pragma unroll
+          for (int k = lane; k < kRank; k += 32) s = fmaf(s_A[i * kRank + k], s_h[n * kRank + k], s);
 #pragma unroll
           for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
           if (lane == 0) {

@@ -25,6 +25,7 @@ struct Plan {
   uint32_t tmem_cols = 0;
   int smem_bytes = 0, smem_w_bytes = 0, ra = 0, Bcap = 0;
   uint32_t rf_warp_mask = 0;
+  int ah_warp = 0;  // recurrent: the warp that computes the CTA's slice of A h each step
   int32_t wl_count[kWarps] = {};
   uint32_t wl[kWarps][kMaxWarpGroups] = {};
 };
@@ -164,6 +165,13 @@ Plan make_plan(int64_t V, int r, int kind, int Bcap, int NH, int sm_count, int s
       if (!place(wl_entry(n_smem + n_tmem + n_rf + i, kTierStream, 0), 9, true)) return false;
     for (int j = 0; j < n_smem; ++j)
       if (!place(wl_entry(j, kTierSmem, 0), 6, true)) return false;
+    // recurrent: the slice of A h goes to the least-loaded warp that keeps no register group (the register warps'
+    // copy of the step loop does not carry that code)
+    if (recurrent) {
+      out.ah_warp = 0;
+      for (int w = 1; w < kWarps; ++w)
+        if (!((out.rf_warp_mask >> w) & 1u) && load[w] < load[out.ah_warp]) out.ah_warp = w;
+    }
     out.ok = true;
     return true;
   };
@@ -495,6 +503,7 @@ int walk_impl(whead_t* h, const float* base, const float* s0, int32_t B, int32_t
   a.smem_w_bytes = pl.smem_w_bytes;
   a.ra = pl.ra;
   a.rf_warp_mask = pl.rf_warp_mask;
+  a.ah_warp = pl.ah_warp;
   std::memcpy(a.wl_count, pl.wl_count, sizeof(a.wl_count));
   std::memcpy(a.wl, pl.wl, sizeof(a.wl));
   const int rc = launch(h, pl, a, NH);
@@ -794,6 +803,7 @@ extern "C" int whead_walk_noalloc(const void* W, const void* E, const whead_para
   a.smem_w_bytes = pl.smem_w_bytes;
   a.ra = pl.ra;
   a.rf_warp_mask = pl.rf_warp_mask;
+  a.ah_warp = pl.ah_warp;
   std::memcpy(a.wl_count, pl.wl_count, sizeof(a.wl_count));
   std::memcpy(a.wl, pl.wl, sizeof(a.wl));
   return noalloc_launch(p.r, NH, tmap, tmap128, stream, nd->smem_optin, pl, a);
