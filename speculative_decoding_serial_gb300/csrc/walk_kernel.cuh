@@ -1304,14 +1304,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint16_t* er = P.E + (int64_t)(0xFFFFFFFFu - (uint32_t)(kk & 0xFFFFFFFFull)) * r;
           for (int off = 0; off < r * 2; off += 128) prefetch_l2(reinterpret_cast<const uint8_t*>(er) + off);
         }
-        // The counter only says when to look: once all but a few CTAs have arrived, every poll also reads the
+        // The counter only says when to look: once all but 64 CTAs have arrived (measured: 96.5 us per walk against
+        // 98.4 when waiting for all but 4; reading every slot from the start was no better), every poll also reads the
         // slots, and the step is complete exactly when every slot carries this step's tag.
         constexpr int kSlotsPerLane = kMaxGrid / 32;
         const unsigned int target = (unsigned int)(t + 1) * (unsigned int)G;
-        const unsigned int near = target - (unsigned int)min(G, 4);
+        const unsigned int near = target - (unsigned int)min(G, 64);
         bool late = false;
         if constexpr (kParRead) {
-          // several walks: this warp waits only until all but a few CTAs have arrived; after the barrier below
+          // several walks: this warp waits only until all but 64 CTAs have arrived; after the barrier below
           // the warps read the slots of their walks side by side
           for (uint32_t spins = 0;; ) {
             unsigned int now = 0;
