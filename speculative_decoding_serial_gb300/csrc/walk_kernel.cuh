@@ -21,11 +21,14 @@
 //  - The fp32 result plus the base logit is the selection key (plus Gumbel noise when T > 0); keys are
 //    packed as ord(key) << 32 | (2^32 - 1 - row) so an unsigned 64-bit maximum picks the largest key
 //    and the smallest row on ties.
-//  - Cross-CTA exchange per step: red.max of the packed key into a step slot, then a release add on an
-//    arrival counter; thread 0 of every CTA polls the counter with acquire loads (bounded by a time
-//    limit) and reads the winners.
+//  - Cross-CTA exchange per step: each CTA stores its winner, tagged with the step, into its own 64-bit
+//    slot (a relaxed store) and adds one to a relaxed arrival counter. Once the counter shows all but 64
+//    CTAs, the readers poll every slot, re-reading those whose tag is not yet the step's, and reduce; the
+//    words carry their own step, so no fence is needed. Several walks are read by several warps at once.
+//    Every wait is bounded by a time limit that ends the walk with a status instead of hanging.
 //  - State advance on the GPU: Markov u <- E[x]; recurrent h <- tanh(A h + E[x] + c) where each CTA
-//    computes a slice of A h before it arrives and every CTA finishes the update redundantly.
+//    computes a slice of A h during the step (published as tagged words) and every CTA finishes the
+//    update redundantly.
 #pragma once
 
 #include <cstdint>
