@@ -89,7 +89,10 @@ class ClockSampler:
     def __init__(self, gpu_id: str):
         self.gpu_id = gpu_id
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        # raw samples go to WHEAD_CLOCK_LOG_DIR when set (to keep them with other run output), else a temp dir
+        import tempfile
+        log_dir = os.environ.get("WHEAD_CLOCK_LOG_DIR") or tempfile.gettempdir()
+        self.path = os.path.join(log_dir, f"whead_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         try:
