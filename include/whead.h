@@ -185,6 +185,22 @@ int whead_status(whead_t* h);
 int whead_plan_info(const whead_t* h, int32_t B, whead_plan* out);
 
 /*
+ * The placement whead_create would choose (Fig. 1: each SM keeps a shard of W; Fig. 12: its split over the
+ * on-chip tiers), computed on the host alone: no device is queried or touched, so it also serves planning
+ * and tests on machines without a GPU. Arguments as in whead_params (max_B, the batch size B in 1..max_B,
+ * flags: only WHEAD_FLAG_W_E4M3 is read) plus the device's SM count and opt-in shared memory per block in
+ * bytes. Fills *out (sm_count as given). work_lists, if not NULL, receives 12 rows of 33 uint32 words, one
+ * row per warp: its number of groups, then up to 32 entries (bits 0..7 the CTA-local group, bits 8..9 its
+ * tier: 0 shared memory, 1 tensor memory, 2 registers, 3 streamed; bits 16..25 its first tensor-memory
+ * column). rf_warp_mask (nullable) receives the warps that keep a group in registers, ah_warp (nullable) the
+ * warp that computes a recurrent head's slice of A h. Returns WHEAD_ERR_INVALID_ARG for bad arguments and
+ * WHEAD_ERR_UNSUPPORTED when the shape is not supported or W cannot be placed.
+ */
+int whead_plan_query(int64_t V, int32_t r, int32_t kind, int32_t max_B, int32_t B, uint32_t flags, int32_t sm_count,
+                     int32_t smem_optin, whead_plan* out, uint32_t* work_lists, uint32_t* rf_warp_mask,
+                     int32_t* ah_warp);
+
+/*
  * E4M3 weights: quantizes W (V x r bf16, device, 16-byte aligned) row by row into Wq (V x r E4M3 codes,
  * device, 16-byte aligned, caller-owned) and sw (V fp32 row scales, device): s = max_k |W[v,k]| / 448 (fp32),
  * Wq[v,k] = E4M3(W[v,k] / s) rounded to nearest even and saturated at +-448; an all-zero row gets s = 0 and

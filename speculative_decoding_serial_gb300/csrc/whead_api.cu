@@ -85,7 +85,9 @@ Plan make_plan(int64_t V, int r, int kind, int Bcap, int NH, int sm_count, int s
   const int64_t ngt = (V + kGroupRows - 1) / kGroupRows;
   const int64_t group_bytes = (int64_t)KB * kBoxBytes;
   const bool recurrent = kind == WHEAD_RECURRENT;
-  const int tmem_max = 128 / KB;
+  // tensor-memory groups: 16 KB columns each, four lane quadrants side by side, within the 512 columns of one
+  // allocation (ceil(n / 4) * 16 * KB <= 512)
+  const int tmem_max = 4 * (32 / KB);
   const int rf_max = (NH == 1) ? 8 : 0;  // at most two register warps per lane quadrant
 
   auto fits = [&](int G, Plan& out, bool allow_stream) -> bool {
@@ -95,6 +97,7 @@ Plan make_plan(int64_t V, int r, int kind, int Bcap, int NH, int sm_count, int s
     const int ra = recurrent ? (r + G - 1) / G : 0;
     const SmemLayout L0 = SmemLayout::make(0, Bcap, r, ra, recurrent, ng, f8);
     const int64_t fixed = 1024 + L0.total;
+    if (fixed > smem_optin) return false;  // e.g. a recurrent head's rows of A on too few CTAs: more CTAs are needed
     const int64_t smem_groups_max = std::min<int64_t>(cap_smem, std::max<int64_t>(0, (smem_optin - fixed) / group_bytes));
     int n_smem = (int)std::min<int64_t>(ng, smem_groups_max);
     int rem = ng - n_smem;
@@ -643,6 +646,43 @@ int whead_plan_info(const whead_t* h, int32_t B, whead_plan* out) {
   out->smem_bytes = pl.smem_bytes;
   out->tmem_cols = (int32_t)pl.tmem_cols;
   out->sm_count = h->sm_count;
+  return WHEAD_OK;
+}
+
+int whead_plan_query(int64_t V, int32_t r, int32_t kind, int32_t max_B, int32_t B, uint32_t flags, int32_t sm_count,
+                     int32_t smem_optin, whead_plan* out, uint32_t* work_lists, uint32_t* rf_warp_mask,
+                     int32_t* ah_warp) {
+  if (!out || (kind != WHEAD_MARKOV && kind != WHEAD_RECURRENT)) return WHEAD_ERR_INVALID_ARG;
+  if (V < 1 || max_B < 1 || max_B > kMaxB || B < 1 || B > max_B || sm_count < 1 || smem_optin < 1)
+    return WHEAD_ERR_INVALID_ARG;
+  if (V >= (int64_t)1 << 24) return WHEAD_ERR_UNSUPPORTED;
+  if (r != 64 && r != 128 && r != 192 && r != 256) return WHEAD_ERR_UNSUPPORTED;
+  const bool f8 = (flags & WHEAD_FLAG_W_E4M3) != 0u;
+  if (f8 && ((r != 128 && r != 256) || max_B > 4)) return WHEAD_ERR_UNSUPPORTED;
+  // the same two plans whead_create makes: up to 8 walks (one n8 half), and up to 16
+  const Plan pl = B <= 8 ? make_plan(V, r, kind, std::min(max_B, 8), 1, sm_count, smem_optin, 0, INT_MAX, INT_MAX,
+                                     INT_MAX, false, f8)
+                         : make_plan(V, r, kind, max_B, 2, sm_count, smem_optin, 0);
+  if (!pl.ok) return WHEAD_ERR_UNSUPPORTED;
+  out->grid = pl.G;
+  out->threads = kThreads;
+  out->groups_per_cta = pl.ng;
+  out->smem_groups = pl.n_smem;
+  out->tmem_groups = pl.n_tmem;
+  out->rf_groups = pl.n_rf;
+  out->stream_groups = pl.n_stream;
+  out->smem_bytes = pl.smem_bytes;
+  out->tmem_cols = (int32_t)pl.tmem_cols;
+  out->sm_count = sm_count;
+  if (work_lists) {
+    for (int w = 0; w < kWarps; ++w) {
+      uint32_t* row = work_lists + (size_t)w * (1 + kMaxWarpGroups);
+      row[0] = (uint32_t)pl.wl_count[w];
+      for (int e = 0; e < kMaxWarpGroups; ++e) row[1 + e] = e < pl.wl_count[w] ? pl.wl[w][e] : 0u;
+    }
+  }
+  if (rf_warp_mask) *rf_warp_mask = pl.rf_warp_mask;
+  if (ah_warp) *ah_warp = pl.ah_warp;
   return WHEAD_OK;
 }
 

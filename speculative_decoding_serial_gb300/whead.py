@@ -88,12 +88,40 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     L.whead_quantize_w_e4m3.argtypes = [vp, i64, i32, vp, vp, vp]
     L.whead_walk_keys.argtypes = [vp, vp, vp, i32, i32, f32, u64, i64, vp, vp, vp, vp]
     L.whead_advance.argtypes = [vp, vp, vp, vp, i32]
+    L.whead_plan_query.argtypes = [i64, i32, i32, i32, i32, ctypes.c_uint32, i32, i32, ctypes.POINTER(WheadPlan), vp,
+                                   vp, vp]
     for name in ("whead_create", "whead_walk", "whead_walk_ex", "whead_walk_host", "whead_status",
                  "whead_plan_info", "whead_destroy", "whead_walk_noalloc",
-                 "whead_set_trace", "whead_quantize_w_e4m3", "whead_walk_keys", "whead_advance"):
+                 "whead_set_trace", "whead_quantize_w_e4m3", "whead_walk_keys", "whead_advance", "whead_plan_query"):
         getattr(L, name).restype = ctypes.c_int
     _lib = L
     return L
+
+
+# tiers of a work-list entry (bits 8..9)
+TIER_SMEM, TIER_TMEM, TIER_RF, TIER_STREAM = 0, 1, 2, 3
+WARPS, MAX_WARP_GROUPS = 12, 32
+
+
+def plan_query(V: int, r: int, kind: int = 0, *, max_B: int = 1, B: int = 1, e4m3: bool = False,
+               sm_count: int, smem_optin: int) -> dict:
+    """whead_plan_query: the placement whead_create would choose, computed on the host (no device needed).
+    Returns the whead_plan fields plus "work_lists" (per warp, its entries as (group, tier, tmem_col)),
+    "rf_warp_mask" and "ah_warp"."""
+    pl = WheadPlan()
+    wl = (ctypes.c_uint32 * (WARPS * (1 + MAX_WARP_GROUPS)))()
+    mask = ctypes.c_uint32(0)
+    ahw = ctypes.c_int32(0)
+    _check(load().whead_plan_query(int(V), int(r), int(kind), int(max_B), int(B), FLAG_W_E4M3 if e4m3 else 0,
+                                   int(sm_count), int(smem_optin), ctypes.byref(pl), ctypes.cast(wl, ctypes.c_void_p),
+                                   ctypes.byref(mask), ctypes.byref(ahw)), "whead_plan_query")
+    out = {n: int(getattr(pl, n)) for n, _ in WheadPlan._fields_}
+    lists = []
+    for w in range(WARPS):
+        row = wl[w * (1 + MAX_WARP_GROUPS):(w + 1) * (1 + MAX_WARP_GROUPS)]
+        lists.append([(e & 0xFF, (e >> 8) & 3, (e >> 16) & 0x3FF) for e in row[1:1 + row[0]]])
+    out.update(work_lists=lists, rf_warp_mask=int(mask.value), ah_warp=int(ahw.value))
+    return out
 
 
 def strerror(code: int) -> str:
