@@ -33,7 +33,7 @@ ERR_INTERNAL = -6
 # Every symbol include/whead.h declares.
 EXPORTS = ("whead_create", "whead_walk", "whead_walk_ex", "whead_walk_host", "whead_status",
            "whead_plan_info", "whead_strerror", "whead_destroy", "whead_walk_noalloc",
-           "whead_set_trace", "whead_quantize_w_e4m3", "whead_walk_keys", "whead_advance")
+           "whead_set_trace", "whead_quantize_w_e4m3", "whead_walk_keys", "whead_advance", "whead_plan_query")
 
 
 class WheadParams(ctypes.Structure):
