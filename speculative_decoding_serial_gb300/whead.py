@@ -80,6 +80,7 @@ def load(build_if_missing: bool = False) -> ctypes.CDLL:
     L.whead_walk_ex.argtypes = [vp, vp, vp, i32, i32, f32, u64, i64, vp, vp, vp]
     L.whead_walk_host.argtypes = [vp, vp, vp, i32, i32, f32, u64, vp, vp]
     L.whead_status.argtypes = [vp]
+    L.whead_set_trace.argtypes = [vp, vp, i64]
     L.whead_plan_info.argtypes = [vp, i32, ctypes.POINTER(WheadPlan)]
     L.whead_strerror.argtypes = [ctypes.c_int]
     L.whead_strerror.restype = ctypes.c_char_p
