@@ -181,18 +181,51 @@ def barrier(world):
         dist.barrier()
 
 
-def oracle_walk_time(d, gamma_sample, repeats):
-    """Wall time of the oracle on `repeats` samples of `gamma_sample` steps of the workload (1 thread)."""
+def oracle_walk_time(d, gamma_sample, repeats, threads=1):
+    """Wall time of the oracle on `repeats` samples of `gamma_sample` steps of the workload, with the rows of each
+    step's projection split over `threads` host threads (the results do not depend on the count)."""
     from oracle import oracle as O
     base = d["base"][:, :gamma_sample].copy()
-    t = time.perf_counter()
-    for _ in range(repeats):
-        O.walk(d["kind"], d["W"], d["E"], base, d["s0"], A=d["A"], c=d["c"], T=d["T"], want_gap=False)
-    return (time.perf_counter() - t) / repeats
+    O.set_threads(threads)
+    try:
+        t = time.perf_counter()
+        for _ in range(repeats):
+            O.walk(d["kind"], d["W"], d["E"], base, d["s0"], A=d["A"], c=d["c"], T=d["T"], want_gap=False)
+        return (time.perf_counter() - t) / repeats
+    finally:
+        O.set_threads(1)
 
 
-def trace_phases(torch, head, base, s0, tok, w, plan, flush, stream, dev, walks=20):
-    """Per-step phase durations from the kernel's phase stamps (median over walks, steps 1.., and CTAs)."""
+def host_cores():
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(d, gamma, name, seconds):
+    """The oracle timed on this host: on all allotted cores (the reported value) and on one thread, each for
+    about half of `seconds` of wall time."""
+    from oracle import oracle as O
+    cores = O.set_threads(host_cores())
+    O.set_threads(1)
+    out = {}
+    for label, threads in (("all", cores), ("one", 1)):
+        one = oracle_walk_time(d, gamma, 1, threads)
+        reps = max(1, min(200, int(math.ceil(seconds / 2 / max(one, 1e-3)))))
+        out[label] = (oracle_walk_time(d, gamma, reps, threads), reps, threads)
+    per, reps, threads = out["all"]
+    per1, reps1, _ = out["one"]
+    return {"value": per * 1e6, "unit": "us/walk", "cores": threads, "kind": "oracle",
+            "sample": f"{reps} full walks of {name} on {threads} host threads (rows of each step split over "
+                      f"the threads); single thread: {reps1} walks",
+            "single_thread": {"value": per1 * 1e6, "unit": "us/walk", "cores": 1}}
+
+
+def trace_phases(torch, head, base, s0, tok, w, plan, flush, stream, dev, walks=20, advance=True):
+    """Per-step phase durations from the kernel's phase stamps (median over walks, steps 1.., and CTAs).
+    advance=False: a fixed-latent walk, whose steps end at the exchange (no advance stamp)."""
     gamma, G = w["gamma"], plan["grid"]
     S = 4 + 8 * gamma
     buf = torch.zeros((G, S), dtype=torch.int64, device=dev)
@@ -209,22 +242,196 @@ def trace_phases(torch, head, base, s0, tok, w, plan, flush, stream, dev, walks=
     half = S // 2
     clk, ns = a[:, :, :half], a[:, :, half:]
     st = lambda t, i: 2 + 4 * t + i
-    proj, exch, adv, skew, step_ns = [], [], [], [], []
+    proj, exch, adv, skew, step_ns, step_clk = [], [], [], [], [], []
     for t in range(1, gamma):
         proj.append(clk[:, :, st(t, 1)] - clk[:, :, st(t, 0)])
         exch.append(clk[:, :, st(t, 2)] - clk[:, :, st(t, 1)])
-        adv.append(clk[:, :, st(t, 3)] - clk[:, :, st(t, 2)])
+        if advance:
+            adv.append(clk[:, :, st(t, 3)] - clk[:, :, st(t, 2)])
         done = ns[:, :, st(t, 1)]
         skew.append(done.max(axis=1) - done.min(axis=1))
-        step_ns.append(ns[:, :, st(t, 3)].max(axis=1) - ns[:, :, st(t - 1, 3)].max(axis=1))
+        step_ns.append(ns[:, :, st(t, 0)].max(axis=1) - ns[:, :, st(t - 1, 0)].max(axis=1))
+        step_clk.append(clk[:, :, st(t, 0)] - clk[:, :, st(t - 1, 0)])
     med = lambda x: float(np.median(np.concatenate([np.ravel(v) for v in x]))) if x else None
     p90 = lambda x: float(np.percentile(np.concatenate([np.ravel(v) for v in x]), 90)) if x else None
     entry_ns = ns[:, :, 1] - ns[:, :, 0]
-    return {"walks": walks, "proj_select_clk": med(proj), "proj_select_clk_p90": p90(proj),
-            "exchange_clk": med(exch), "advance_clk": med(adv), "arrival_skew_ns": med(skew),
-            "step_ns": med(step_ns), "entry_ns_median": float(np.median(entry_ns)),
+    last = st(gamma - 1, 2)  # every walk stamps the end of its last exchange
+    span_clk, span_ns = clk[:, :, last] - clk[:, :, 0], ns[:, :, last] - ns[:, :, 0]
+    ok = span_ns > 0
+    mhz = float(np.median(span_clk[ok] / span_ns[ok] * 1e3)) if ok.any() else None
+    phase_sum = med(proj) + med(exch) + (med(adv) if adv else 0.0) if proj else None
+    return {"walks": walks, "kernel_sm_mhz": mhz, "proj_select_clk": med(proj), "proj_select_clk_p90": p90(proj),
+            "exchange_clk": med(exch), "advance_clk": med(adv), "step_clk": med(step_clk),
+            "arrival_skew_ns": med(skew), "step_ns": med(step_ns), "entry_ns_median": float(np.median(entry_ns)),
             "entry_ns_max": float(np.median(entry_ns.max(axis=1))),
-            "exchange_share": (med(exch) / (med(proj) + med(exch) + med(adv))) if proj else None}
+            "exchange_share": (med(exch) / phase_sum) if proj else None}
+
+
+def fit_line(xs, ys):
+    """Least-squares slope and intercept (Fig. 11's method: slope = per-step cost, intercept = entry)."""
+    xm, ym = sum(xs) / len(xs), sum(ys) / len(ys)
+    sl = sum((a - xm) * (b - ym) for a, b in zip(xs, ys)) / sum((a - xm) ** 2 for a in xs)
+    return sl, ym - sl * xm
+
+
+def fixed_latent(args):
+    """Fig. 13b of the pages on GB300: complete calls and disjoint per-step costs of the Markov (16 steps) and
+    recurrent (15 steps) heads, each with the state advance and as the fixed-latent probe (WHEAD_FLAG_FIXED_LATENT:
+    projection and selection repeated on the unchanged initial state). Per-step cost = least-squares slope of the
+    walk time over gamma in {1, 7, gamma}; phases from the kernel's stamps. One JSON line per head and mode."""
+    import numpy as np
+    import torch
+
+    import whead_inputs as I
+    from speculative_decoding_serial_gb300 import build
+    from speculative_decoding_serial_gb300 import whead as wh
+
+    build.build()
+    dev = torch.device("cuda", 0)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+    for name in ("markov_v151936_r256_b1_g16", "recurrent_v151936_r256_b1_g15"):
+        w = I.WORKLOADS[name]
+        d = I.workload_inputs(name)
+        B, G16 = w["B"], w["gamma"]
+        W = torch.from_numpy(d["W"].view(np.int16)).view(torch.bfloat16).to(dev)
+        E = torch.from_numpy(d["E"].view(np.int16)).view(torch.bfloat16).to(dev)
+        base = torch.from_numpy(d["base"]).to(dev)
+        s0 = torch.from_numpy(d["s0"]).to(dev)
+        A = None if d["A"] is None else torch.from_numpy(d["A"]).to(dev)
+        c = None if d["c"] is None else torch.from_numpy(d["c"]).to(dev)
+        gammas = [1, 7, G16]
+        for mode, flags in (("walk", 0), ("fixed_latent", wh.FLAG_FIXED_LATENT)):
+            head = wh.Head(W, E, kind=w["kind"], A=A, c=c, max_B=B, max_gamma=G16, stream=stream, flags=flags)
+            plan = head.plan(B)
+            ys = []
+            for g in gammas:
+                bg = base[:, :g].contiguous()
+                tok = torch.empty((B, g), dtype=torch.int32, device=dev)
+                for _ in range(3):
+                    head.walk(bg, s0, T=w["T"], out_tokens=tok)
+                ts = []
+                for _ in range(args.sweep_walks):
+                    flush.zero_()
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    head.walk(bg, s0, T=w["T"], out_tokens=tok)
+                    e1.record(stream)
+                    e1.synchronize()
+                    ts.append(e0.elapsed_time(e1) * 1e3)
+                ys.append(statistics.median(ts))
+            tok = torch.empty((B, G16), dtype=torch.int32, device=dev)
+            phases = trace_phases(torch, head, base, s0, tok, w, plan, flush, stream, dev, advance=(flags == 0))
+            status = head.status()
+            head.close()
+            sl, ic = fit_line(gammas, ys)
+            print(json.dumps({"fig13b": mode, "workload": name, "status": status, "gammas": gammas,
+                              "us_per_walk": ys, "us_per_step_slope": sl, "entry_intercept_us": ic,
+                              "phases": phases, "placement": plan}), flush=True)
+
+
+def sharded_measure(walk, merge_once, steps, warmup, world, timer):
+    """Rank logic of the sharded leg. walk(): one whole walk of this rank's shard (all ranks call it together;
+    returns the tokens); merge_once(): one all-reduce of a step's packed keys; timer(fn) -> seconds that fn took
+    on this rank's device (CUDA events) or host. Returns seconds per walk and per merge, each the maximum over
+    ranks, and the last walk's tokens."""
+    for _ in range(warmup):
+        walk()
+    out = {}
+    barrier(world)
+    out["walk_s"] = max_over_ranks(timer(lambda: [out.__setitem__("tokens", walk()) for _ in range(steps)]),
+                                   world) / steps
+    barrier(world)
+    out["merge_s"] = max_over_ranks(timer(lambda: [merge_once() for _ in range(steps)]), world) / steps
+    return out
+
+
+def sharded(args, world, rank, local):
+    """Vocabulary sharding (the one exchange the method has across GPUs: Fig. 8's packed selection taken over
+    ranks). With N > 1 ranks (torchrun, NCCL) rank k holds rows shard_bounds(V, N, k) of W and walks them step by
+    step: a one-step walk of its shard, an all-reduce MAX of B packed keys, the state advanced on its GPU. With
+    one process, --shards K shards of the vocabulary run in lockstep on the one GPU (their keys merged on the
+    device), which measures the protocol's per-step cost without the link. One JSON line (rank 0)."""
+    import numpy as np
+    import torch
+
+    import whead_inputs as I
+    from speculative_decoding_serial_gb300 import build
+    from speculative_decoding_serial_gb300 import sharded as S
+    from speculative_decoding_serial_gb300 import whead as wh
+
+    if rank == 0 or not build.needs_build():
+        build.build()
+    barrier(world)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    name = args.workload
+    w = I.WORKLOADS[name]
+    d = I.workload_inputs(name)
+    B, gamma, V, r = w["B"], w["gamma"], w["V"], w["r"]
+    W = torch.from_numpy(d["W"].view(np.int16)).view(torch.bfloat16).to(dev)
+    E = torch.from_numpy(d["E"].view(np.int16)).view(torch.bfloat16).to(dev)
+    base = torch.from_numpy(d["base"]).to(dev)
+    s0 = torch.from_numpy(d["s0"]).to(dev)
+    A = None if d["A"] is None else torch.from_numpy(d["A"]).to(dev)
+    c = None if d["c"] is None else torch.from_numpy(d["c"]).to(dev)
+    nshards = world if world > 1 else max(1, args.shards)
+    mine = [rank] if world > 1 else list(range(nshards))
+    heads, bases, bounds = [], [], []
+    for k in mine:
+        lo, hi = S.shard_bounds(V, nshards, k)
+        heads.append(wh.Head(W[lo:hi].contiguous(), E, kind=w["kind"], A=A, c=c, max_B=B, max_gamma=1, v_offset=lo,
+                             e_rows=V, stream=stream))
+        bases.append([base[:, t:t + 1, lo:hi].contiguous() for t in range(gamma)])
+        bounds.append((lo, hi))
+    keys = torch.empty((B, 1), dtype=torch.int64, device=dev)
+    tok1 = torch.empty((B, 1), dtype=torch.int32, device=dev)
+    merge = S.allreduce_max() if world > 1 else (lambda v: v)
+
+    def step(t, s):
+        got = []
+        for h, bs in zip(heads, bases):
+            h.walk_keys(bs[t], s, T=w["T"], seed=0, t0=t, out_tokens=tok1, out_keys=keys)
+            got.append(S.to_ordered(keys[:, 0]))
+        local_max = got[0] if len(got) == 1 else torch.stack(got).max(dim=0).values
+        return S.from_ordered(local_max)
+
+    def advance(x, s):
+        return heads[0].advance(x.contiguous(), s, torch.empty_like(s))
+
+    proto = S.ShardedWalk(step, merge, advance)
+    probe = torch.zeros((B,), dtype=torch.int64, device=dev)
+
+    def timer(fn):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize(dev)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) * 1e-3
+
+    m = sharded_measure(lambda: proto.walk(s0, gamma)[0], lambda: merge(probe), args.steps, max(3, args.warmup),
+                        world, timer)
+    status = max(h.status() for h in heads)
+    tokens = m["tokens"].cpu().numpy()
+    # the unsharded walk of the same inputs, for the tokens and the comparison
+    full = wh.Head(W, E, kind=w["kind"], A=A, c=c, max_B=B, max_gamma=gamma, stream=stream)
+    ref_tok = full.walk(base, s0, T=w["T"], seed=0).cpu().numpy()
+    full.close()
+    for h in heads:
+        h.close()
+    if rank != 0:
+        return
+    print(json.dumps({
+        "sharded": name, "n_gpus": world, "shards": nshards, "mode": "ranks (NCCL)" if world > 1 else
+        "shards in lockstep on one GPU", "rows_per_shard": [b[1] - b[0] for b in bounds] if world == 1 else
+        [S.shard_bounds(V, world, k)[1] - S.shard_bounds(V, world, k)[0] for k in range(world)],
+        "us_per_walk": m["walk_s"] * 1e6, "us_per_step": m["walk_s"] * 1e6 / gamma,
+        "allreduce_us_per_step": m["merge_s"] * 1e6 if world > 1 else None, "walks": args.steps,
+        "tokens_equal_unsharded_walk": bool((tokens == ref_tok).all()), "status": status,
+        "launches_per_walk": gamma * (len(heads) + 1)}), flush=True)
 
 
 def reference_arm(args, world, rank):
@@ -235,6 +442,7 @@ def reference_arm(args, world, rank):
     from oracle import oracle as O
     w = I.WORKLOADS[args.workload]
     d = I.workload_inputs(args.workload)
+    cores = O.set_threads(host_cores())  # rows of each step over every allotted core (same results)
     base1 = d["base"][:, :1].copy()
     for _ in range(args.warmup):
         O.walk(d["kind"], d["W"], d["E"], base1, d["s0"], A=d["A"], c=d["c"], T=d["T"], want_gap=False)
@@ -244,14 +452,16 @@ def reference_arm(args, world, rank):
         O.walk(d["kind"], d["W"], d["E"], d["base"][:, k % w["gamma"]:k % w["gamma"] + 1].copy(), s0, A=d["A"],
                c=d["c"], T=d["T"], t0=k % w["gamma"], want_gap=False)
     per_step = (time.perf_counter() - t) / args.steps
+    O.set_threads(1)
     value = per_step * w["gamma"] * 1e6
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "us/walk", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": args.workload, **{k: w[k] for k in ("V", "r", "B", "gamma", "T")}},
-        "cpu_baseline": {"value": value, "unit": "us/walk", "cores": 1, "kind": "oracle",
-                         "sample": f"{args.steps} single walk steps of the workload (x{w['gamma']} for a walk)"},
+        "cpu_baseline": {"value": value, "unit": "us/walk", "cores": cores, "kind": "oracle",
+                         "sample": f"{args.steps} single walk steps of the workload (x{w['gamma']} for a walk), "
+                                   f"rows of each step split over {cores} host threads"},
         "e2e": {"value": value, "unit": "us/walk", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -352,6 +562,11 @@ def ours(args, world, rank, local):
     peak = alg_bytes / (t_roof_us * 1e3)
 
     phases = trace_phases(torch, head, base, s0, tok, w, plan, flush, stream, dev)
+    clocks["kernel_sm_mhz"] = phases.pop("kernel_sm_mhz")
+    clocks["kernel_sm_mhz_source"] = ("clock64 / globaltimer stamps of every CTA over the traced walks run right "
+                                      "after the timed region (the timed region is shorter than one nvidia-smi "
+                                      "sample)")
+    traffic = recorded_traffic() if args.workload == DEFAULT_WORKLOAD else None
 
     # end to end through the host-buffer entry point: pinned inputs copied in, tokens copied out
     base_h = torch.from_numpy(d["base"]).pin_memory()
@@ -371,11 +586,7 @@ def ours(args, world, rank, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        one = oracle_walk_time(d, gamma, 1)
-        reps = max(1, min(50, int(math.ceil(args.cpu_seconds / max(one, 1e-3)))))
-        per = oracle_walk_time(d, gamma, reps)
-        cpu = {"value": per * 1e6, "unit": "us/walk", "cores": 1, "kind": "oracle",
-               "sample": f"{reps} full walks of {args.workload} (single thread)"}
+        cpu = cpu_baseline(d, gamma, args.workload, args.cpu_seconds)
 
     head.close()
     if rank != 0:
@@ -388,7 +599,10 @@ def ours(args, world, rank, local):
                    "l2": "flushed (256 MB write) before every timed walk", "placement": plan},
         "roofline": {"bound": "onchip", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": t_roof_us / us_per_walk,
-                     "traffic": recorded_traffic() if args.workload == DEFAULT_WORKLOAD else None,
+                     "traffic": traffic,
+                     "traffic_source": ("ncu dram__bytes_read.sum + dram__bytes_write.sum of one launch, from the "
+                                        "committed profile taken on this kernel source (sha-matched)")
+                     if traffic is not None else None,
                      "t_roof_us": t_roof_us, "t_entry_us": t_entry_us, "t_star_clk_per_step": t_star_clk,
                      "hbm_peak_gbs": hbm_gbs, "hbm_peak_kind": peak_kind, "clock_mhz": mhz,
                      "onchip_measured": onchip,
@@ -616,9 +830,17 @@ def main():
     ap.add_argument("--sweep-walks", type=int, default=100)
     ap.add_argument("--ablation", action="store_true", help="fusion vs residency (resident / fused streaming / step-wise)")
     ap.add_argument("--placement", action="store_true", help="placement sweep over shared/tensor/register tiers")
+    ap.add_argument("--fixed-latent", action="store_true",
+                    help="per-step cost with and without the state advance (Markov and recurrent heads)")
+    ap.add_argument("--sharded", action="store_true",
+                    help="vocabulary sharded over the ranks (or --shards K shards in lockstep on one GPU)")
+    ap.add_argument("--shards", type=int, default=2)
     args = ap.parse_args()
     if args.placement:
         placement(args)
+        return
+    if args.fixed_latent:
+        fixed_latent(args)
         return
     if args.sweep:
         sweep(args)
@@ -628,7 +850,9 @@ def main():
         return
     args.warmup = max(3, args.warmup)
     world, rank, local = dist_setup(args)
-    if args.impl == "reference":
+    if args.sharded:
+        sharded(args, world, rank, local)
+    elif args.impl == "reference":
         reference_arm(args, world, rank)
     else:
         ours(args, world, rank, local)

@@ -203,8 +203,9 @@ int whead_plan_query(int64_t V, int32_t r, int32_t kind, int32_t max_B, int32_t 
 /*
  * E4M3 weights: quantizes W (V x r bf16, device, 16-byte aligned) row by row into Wq (V x r E4M3 codes,
  * device, 16-byte aligned, caller-owned) and sw (V fp32 row scales, device): s = max_k |W[v,k]| / 448 (fp32),
- * Wq[v,k] = E4M3(W[v,k] / s) rounded to nearest even and saturated at +-448; an all-zero row gets s = 0 and
- * zero codes. Enqueued on `stream` (cudaStream_t, NULL = legacy default). r must be 128 or 256.
+ * inv = 1 / s (fp32, correctly rounded, formed once per row), Wq[v,k] = E4M3(W[v,k] * inv) rounded to nearest
+ * even and saturated at +-448; a row whose largest magnitude is below 448 * FLT_MIN (inv would not be finite)
+ * gets s = 0 and zero codes. Enqueued on `stream` (cudaStream_t, NULL = legacy default). r must be 128 or 256.
  * Returns WHEAD_ERR_INVALID_ARG for null or misaligned pointers, WHEAD_ERR_UNSUPPORTED for other shapes.
  */
 int whead_quantize_w_e4m3(const void* W, int64_t V, int32_t r, void* Wq, float* sw, void* stream);
@@ -228,11 +229,16 @@ int whead_destroy(whead_t* h);
  * plans for its own B and gamma; params->stream is the stream used); base, u0, B, gamma, T, seed,
  * out_tokens and out_logits as for whead_walk. out_status: NULL, or a device int32 that receives the
  * call's device status (0, or WHEAD_ERR_TIMEOUT / WHEAD_ERR_INTERNAL) once the stream reaches the end of
- * the walk. All pointers are device pointers owned by the caller.
+ * the walk. With out_status NULL a device-side failure is not reported anywhere (the call has already
+ * returned WHEAD_OK and the tokens are then undefined): pass a status word to learn of it. All pointers are
+ * device pointers owned by the caller.
  *
  * Errors: WHEAD_ERR_INVALID_ARG / WHEAD_ERR_UNSUPPORTED as whead_create and whead_walk; a call whose
  * scratch would exceed WHEAD_NOALLOC_SCRATCH_BYTES is rejected with WHEAD_ERR_UNSUPPORTED: more than 16
- * walks, more than 64 steps, or a grid of more than 256 CTAs (more SMs than this array has slots for).
+ * walks or more than 64 steps. The grid is at most 256 CTAs (the array's slots per step); on a device with
+ * more SMs the walk uses 256 of them. The measurement and staging flags (WHEAD_FLAG_FORCE_STREAM,
+ * WHEAD_FLAG_PLACEMENT_CAPS, WHEAD_FLAG_HOST_STAGE) and WHEAD_FLAG_W_E4M3 need a handle and are rejected
+ * with WHEAD_ERR_UNSUPPORTED.
  *
  * Every call shares the one array and clears what must start at zero (exchange slots, counter, status and,
  * for the recurrent head, the tagged A h slices) with cudaMemsetAsync on the call's stream. Calls whose walks overlap on the GPU (different streams, or several

@@ -30,14 +30,22 @@ RECURRENT = 1
 
 
 def build(force: bool = False) -> str:
-    """Compile the oracle with gcc (no FMA contraction, so x86 and Arm hosts agree bit for bit)."""
+    """Compile the oracle with gcc (no FMA contraction, so x86 and Arm hosts agree bit for bit). OpenMP splits
+    a step's rows over threads when the compiler has it; otherwise the oracle builds single-threaded."""
     os.makedirs(_BUILD, exist_ok=True)
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
         tmp = _LIB + f".tmp{os.getpid()}"
-        subprocess.run(["gcc", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"],
-                       check=True)
+        base = ["gcc", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+        if subprocess.run(base[:3] + ["-fopenmp"] + base[3:], capture_output=True).returncode != 0:
+            subprocess.run(base, check=True)
         os.replace(tmp, _LIB)
     return _LIB
+
+
+def set_threads(n: int) -> int:
+    """Threads for the rows of each step's projection (1 by default); returns the number in use. The results
+    are the same for every thread count."""
+    return int(lib().whead_oracle_set_threads(int(n)))
 
 
 def lib() -> ctypes.CDLL:
@@ -54,6 +62,8 @@ def lib() -> ctypes.CDLL:
             L.whead_oracle_uniform.restype = ctypes.c_float
             L.whead_oracle_gumbel.argtypes = [ctypes.c_uint64, ctypes.c_int32, ctypes.c_int64, ctypes.c_int64]
             L.whead_oracle_gumbel.restype = ctypes.c_float
+            L.whead_oracle_set_threads.argtypes = [ctypes.c_int]
+            L.whead_oracle_set_threads.restype = ctypes.c_int
             L.whead_oracle_bf16_round.argtypes = [ctypes.c_float]
             L.whead_oracle_bf16_round.restype = ctypes.c_uint16
             vp = ctypes.c_void_p

@@ -31,14 +31,35 @@
  * SC'11) with key (seed lo, seed hi) and counter (v/4, tau, b, 0), word v%4; U = ((w>>9)+0.5)*2^-23;
  * g = -logf(-logf(U)).
  *
- * Build: gcc -O2 -ffp-contract=off -fPIC -shared whead_oracle.c -lm  (no FMA contraction, so that x86
- * and Arm hosts give the same bits).
+ * Build: gcc -O2 -ffp-contract=off -fopenmp -fPIC -shared whead_oracle.c -lm  (no FMA contraction, so that
+ * x86 and Arm hosts give the same bits). OpenMP only splits the rows v of a step's projection over threads
+ * (whead_oracle_set_threads, default one thread): every row is computed by the same code in the same order
+ * whichever thread takes it, so the results do not depend on the thread count. Without OpenMP the file
+ * builds single-threaded.
  */
 #include <float.h>
 #include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+static int g_threads = 1; /* threads for the rows of a step's projection */
+
+/* Sets the number of threads the walk's projection uses (>= 1; clamped to what OpenMP offers); returns the
+ * number now in use (1 when the file was built without OpenMP). */
+int whead_oracle_set_threads(int n) {
+#ifdef _OPENMP
+  const int cap = omp_get_num_procs();
+  g_threads = n < 1 ? 1 : (n > cap ? cap : n);
+#else
+  (void)n;
+  g_threads = 1;
+#endif
+  return g_threads;
+}
 
 #define ORACLE_OK 0
 #define ORACLE_EINVAL (-1)
@@ -241,7 +262,11 @@ static int walk_impl(int fp8, int32_t kind, int64_t V, int32_t r, const uint16_t
         }
       }
 
-      /* projection, base add, emitted logits, selection keys */
+      /* projection, base add, emitted logits, selection keys (rows are independent: each thread takes whole
+         rows and every row's arithmetic is the same whichever thread runs it) */
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static) num_threads(g_threads) if (g_threads > 1)
+#endif
       for (int64_t v = 0; v < V; ++v) {
         double p = 0.0;
         if (!fp8) {

@@ -3,7 +3,8 @@
 // Built as a separate library (libwhead_probe.so) for the benchmark; the walk library does not use it.
 //   whead_probe_onchip(out[6]):
 //     out[0] shared-memory read bandwidth, bytes per SM clock (ld.shared.v4, 384 threads, 192 KB resident)
-//     out[1] tensor-memory read bandwidth, bytes per SM clock (tcgen05.ld.32x32b.x32, 384 threads, 512 cols)
+//     out[1] tensor-memory read bandwidth, bytes per SM clock (two tcgen05.ld.32x32b.x64 in flight per wait,
+//            384 threads, 512 columns)
 //     out[2] SM clocks per mma.sync.m16n8k16 bf16 -> fp32 per SM (independent accumulators, 384 threads)
 //     out[3] SM clocks per grid-wide arrival + wait over all SMs (relaxed counter; cooperative launch)
 //     out[4] SM clocks per tcgen05.mma.cta_group::1.kind::f16 of shape M128 N16 K16 (A and B in shared memory,
@@ -43,6 +44,23 @@ __global__ void __launch_bounds__(kThreads, 1) smem_bw(uint32_t* out, long long*
   if (threadIdx.x == 0) cyc[blockIdx.x] = t1 - t0;
 }
 
+// 64 columns of this warp's lane quadrant in one load (32 lanes x 64 x 4 B = 8 KB per warp)
+#define WH_TMEM_X64_OUT(r)                                                                                          \
+  "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),      \
+      "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),       \
+      "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),      \
+      "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]),      \
+      "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]),      \
+      "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]),      \
+      "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]),      \
+      "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+#define WH_TMEM_X64_ASM                                                                                             \
+  "tcgen05.ld.sync.aligned.32x32b.x64.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"  \
+  "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47," \
+  "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];"
+
+// Tensor-memory read bandwidth with loads kept in flight: each warp issues two 64-column loads (16 KB) and waits
+// once, sweeping all 512 columns of its lane quadrant (the three warps of a quadrant each read all of them).
 __global__ void __launch_bounds__(kThreads, 1) tmem_bw(uint32_t* out, long long* cyc, int iters) {
   __shared__ uint32_t taddr_s;
   const int warp = threadIdx.x >> 5;
@@ -55,24 +73,18 @@ __global__ void __launch_bounds__(kThreads, 1) tmem_bw(uint32_t* out, long long*
   __syncthreads();
   asm volatile("tcgen05.fence::after_thread_sync;");
   const uint32_t taddr = taddr_s;
-  const int quad = warp & 3, grp = warp >> 2, ngrp = (blockDim.x >> 5) >> 2;
+  const int quad = warp & 3;
   const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
   uint32_t acc = 0;
   const long long t0 = clock64();
   for (int it = 0; it < iters; ++it) {
-    for (int col = grp * 32; col < 512; col += ngrp * 32) {
-      uint32_t r[32];
-      asm volatile(
-          "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
-          "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-          : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
-            "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
-            "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-            "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-          : "r"(taddr + lane_base + (uint32_t)col));
+    for (int col = 0; col < 512; col += 128) {
+      uint32_t r0[64], r1[64];
+      asm volatile(WH_TMEM_X64_ASM : WH_TMEM_X64_OUT(r0) : "r"(taddr + lane_base + (uint32_t)col));
+      asm volatile(WH_TMEM_X64_ASM : WH_TMEM_X64_OUT(r1) : "r"(taddr + lane_base + (uint32_t)(col + 64)));
       asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-      for (int j = 0; j < 32; ++j) acc ^= r[j];
+      for (int j = 0; j < 64; ++j) acc ^= r0[j] ^ r1[j];
     }
   }
   asm volatile("tcgen05.fence::before_thread_sync;");
@@ -82,6 +94,8 @@ __global__ void __launch_bounds__(kThreads, 1) tmem_bw(uint32_t* out, long long*
   out[blockIdx.x * blockDim.x + threadIdx.x] = acc;
   if (threadIdx.x == 0) cyc[blockIdx.x] = t1 - t0;
 }
+#undef WH_TMEM_X64_ASM
+#undef WH_TMEM_X64_OUT
 
 __global__ void __launch_bounds__(kThreads, 1) mma_rate(float* out, long long* cyc, int iters) {
   const uint32_t a0 = threadIdx.x, a1 = threadIdx.x * 3u, a2 = threadIdx.x * 5u, a3 = threadIdx.x * 7u;
@@ -255,7 +269,7 @@ extern "C" int whead_probe_onchip(double* out) {
     tmem_bw<<<nsm, kThreads, 160 * 1024>>>(d_out, d_cyc, 2);
     tmem_bw<<<nsm, kThreads, 160 * 1024>>>(d_out, d_cyc, it_tmem);
     if (cudaDeviceSynchronize() != cudaSuccess) { rc = -4; break; }
-    out[1] = (double)it_tmem * 512 * 128 * 4 / median_cycles(d_cyc, nsm);
+    out[1] = (double)it_tmem * (kThreads / 128) * 512 * 128 * 4 / median_cycles(d_cyc, nsm);
     const int it_mma = 2000;
     mma_rate<<<nsm, kThreads>>>(reinterpret_cast<float*>(d_out), d_cyc, 10);
     mma_rate<<<nsm, kThreads>>>(reinterpret_cast<float*>(d_out), d_cyc, it_mma);

@@ -57,7 +57,6 @@ constexpr int kStatusInternal = -6;
 
 constexpr uint32_t kFlagLogitsF32 = 1u << 0;
 constexpr uint32_t kFlagFixedLatent = 1u << 1;
-constexpr uint32_t kFlagForceStream = 1u << 2;
 constexpr uint32_t kFlagSkipArrival = 1u << 8;
 constexpr uint32_t kFlagBaseAsync = 1u << 24;  // set by the library: next step's base logits copied during a step
 

@@ -771,7 +771,9 @@ extern "C" int whead_walk_noalloc(const void* W, const void* E, const whead_para
   if (p.V >= (int64_t)1 << 24) return WHEAD_ERR_UNSUPPORTED;
   if (p.r != 64 && p.r != 128 && p.r != 192 && p.r != 256) return WHEAD_ERR_UNSUPPORTED;
   if (p.kind == WHEAD_RECURRENT && !p.A) return WHEAD_ERR_UNSUPPORTED;
-  if (p.flags & WHEAD_FLAG_W_E4M3) return WHEAD_ERR_UNSUPPORTED;  // needs the handle's quantized copy of W
+  // E4M3 needs the handle's quantized copy of W; the measurement and staging modes need a handle's plans
+  if (p.flags & (WHEAD_FLAG_W_E4M3 | WHEAD_FLAG_FORCE_STREAM | WHEAD_FLAG_PLACEMENT_CAPS | WHEAD_FLAG_HOST_STAGE))
+    return WHEAD_ERR_UNSUPPORTED;
   if (p.v_offset < 0 || (p.v_offset & 15)) return WHEAD_ERR_INVALID_ARG;
   if (p.v_offset + p.V >= (int64_t)1 << 24) return WHEAD_ERR_UNSUPPORTED;
   if (!(T >= 0.0f) || T > 3.0e38f) return WHEAD_ERR_INVALID_ARG;
@@ -789,7 +791,7 @@ extern "C" int whead_walk_noalloc(const void* W, const void* E, const whead_para
   const int NH = B <= 8 ? 1 : 2;
   const Plan pl = make_plan(p.V, p.r, p.kind, B, NH, nd->sm_count, nd->smem_optin, 0);
   if (!pl.ok) return WHEAD_ERR_UNSUPPORTED;
-  if (pl.G > kNaMaxGrid) return WHEAD_ERR_UNSUPPORTED;  // more CTAs than the array has slots for
+  static_assert(kMaxGrid <= kNaMaxGrid, "the planner caps the grid at the array's slots per step");
 
   CUtensorMap tmap, tmap128;
   if (encode_w(&tmap, W, p.V, p.r, kGroupRows) != WHEAD_OK) return WHEAD_ERR_CUDA;

@@ -254,13 +254,17 @@ class Head:
 
 
 def walk_noalloc(W, E, base, u0, *, kind=MARKOV, A=None, c=None, T=0.0, seed=0, flags=0, timeout_us=0,
-                 out_tokens, out_logits=None, out_status=None, stream=None):
+                 out_tokens, out_logits=None, out_status=None, stream=None, check=False):
     """The allocation-free walk (whead_walk_noalloc): every buffer, outputs included, comes from the caller.
 
     For callers that must not allocate device memory (an engine that owns all GPU memory in its own pool,
     or a loop that cannot afford the device synchronization of cudaMalloc). The library's scratch for this
     call is a fixed device array shared by all calls, so walks issued through this function must not
     overlap on the GPU. The first call on a device should come before any stream capture.
+
+    out_status: a device int32 tensor that receives the walk's device status. Without it a time-out or
+    internal error on the device is not reported anywhere. check=True (which needs out_status) waits for the
+    stream and raises WheadError when the status is not 0.
     """
     import torch
     B, gamma, V = base.shape
@@ -268,7 +272,12 @@ def walk_noalloc(W, E, base, u0, *, kind=MARKOV, A=None, c=None, T=0.0, seed=0, 
     s = torch.cuda.current_stream() if stream is None else stream
     p = WheadParams(kind=int(kind), r=r, V=int(V), A=_ptr(A), c=_ptr(c), max_B=int(B), max_gamma=int(gamma),
                     stream=ctypes.c_void_p(s.cuda_stream), flags=int(flags), grid=0, timeout_us=int(timeout_us))
+    if check and out_status is None:
+        raise ValueError("check=True needs out_status")
     _check(load().whead_walk_noalloc(_ptr(W), _ptr(E), ctypes.byref(p), _ptr(base), _ptr(u0), int(B), int(gamma),
                                      float(T), int(seed) & (2**64 - 1), _ptr(out_tokens), _ptr(out_logits),
                                      _ptr(out_status)), "whead_walk_noalloc")
+    if check:
+        s.synchronize()
+        _check(int(out_status.item()), "whead_walk_noalloc (device status)")
     return out_tokens

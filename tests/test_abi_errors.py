@@ -104,6 +104,9 @@ NOALLOC_CASES = [
     (dict(r=100), dict(), wh.ERR_UNSUPPORTED),
     (dict(V=1 << 24), dict(), wh.ERR_UNSUPPORTED),
     (dict(flags=wh.FLAG_W_E4M3), dict(), wh.ERR_UNSUPPORTED),  # needs a handle's quantized copy of W
+    (dict(flags=wh.FLAG_FORCE_STREAM), dict(), wh.ERR_UNSUPPORTED),     # measurement modes need a handle's plans
+    (dict(flags=wh.FLAG_PLACEMENT_CAPS), dict(), wh.ERR_UNSUPPORTED),
+    (dict(flags=wh.FLAG_HOST_STAGE), dict(), wh.ERR_UNSUPPORTED),       # a host-buffer option; no host buffers here
     (dict(kind=wh.RECURRENT), dict(), wh.ERR_UNSUPPORTED),
     (dict(v_offset=8), dict(), wh.ERR_INVALID_ARG),
     (dict(), dict(u0=FAKE_ODD), wh.ERR_INVALID_ARG),

@@ -327,3 +327,37 @@ def test_invalid_arguments_rejected():
         O.walk(RECURRENT, W, E, base, s0)          # recurrent head without A
     with pytest.raises(ValueError):
         O.walk(MARKOV, W, E, base, s0, T=-1.0)
+
+
+def test_walk_prefix_is_the_shorter_walk():
+    """A walk's first steps do not depend on later base logits (Fig. 2: each step uses only the state the
+    earlier steps produced): the first g steps of a gamma-step walk equal the g-step walk, sampled or not."""
+    for kind, T in ((MARKOV, 0.0), (MARKOV, 1.0), (RECURRENT, 0.7)):
+        d = I.make_inputs(kind, 300, 32, 3, 7, seed=21)
+        full = O.walk(kind, d["W"], d["E"], d["base"], d["s0"], A=d["A"], c=d["c"], T=T, seed=4, want_state=True)
+        for g in (1, 3):
+            part = O.walk(kind, d["W"], d["E"], np.ascontiguousarray(d["base"][:, :g]), d["s0"], A=d["A"], c=d["c"],
+                          T=T, seed=4, want_state=True)
+            np.testing.assert_array_equal(part["tokens"], full["tokens"][:, :g])
+            np.testing.assert_array_equal(part["state"], full["state"][:, :g])
+
+
+@pytest.mark.parametrize("kind,T,e4m3", [(MARKOV, 0.0, False), (MARKOV, 1.0, False), (RECURRENT, 0.7, False),
+                                          (MARKOV, 1.0, True)])
+def test_thread_count_does_not_change_results(kind, T, e4m3):
+    """The oracle may split a step's rows over threads (OpenMP); every output must be bit-identical to the
+    single-threaded walk."""
+    d = I.make_inputs(kind, 5003, 128, 2, 4, seed=8)
+    w8 = O.quantize_w_e4m3(d["W"]) if e4m3 else None
+    kw = dict(A=d["A"], c=d["c"], T=T, seed=3, want_logits=True, want_z=True, want_gap=True, want_state=True,
+              w_e4m3=w8)
+    try:
+        assert O.set_threads(1) == 1
+        one = O.walk(kind, d["W"], d["E"], d["base"], d["s0"], **kw)
+        n = O.set_threads(4)
+        many = O.walk(kind, d["W"], d["E"], d["base"], d["s0"], **kw)
+    finally:
+        O.set_threads(1)
+    print(f"threads used: {n}")
+    for k in one:
+        np.testing.assert_array_equal(one[k], many[k], err_msg=k)

@@ -31,7 +31,7 @@ def _pack(key, v):
     return k - (1 << 64) if k >= (1 << 63) else k  # the uint64's bits as int64
 
 
-def _rank_main(rank, world, port, kind, T, q):
+def _rank_main(rank, world, port, kind, T, q, via_bench=False):
     import torch
     import torch.distributed as dist
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world))
@@ -69,7 +69,23 @@ def _rank_main(rank, world, port, kind, T, q):
         return torch.from_numpy(np.tanh(pre).astype(np.float32))
 
     walk = S.ShardedWalk(step, S.allreduce_max(), advance)
-    toks, states = walk.walk(torch.from_numpy(d["s0"].copy()), G)
+    s0 = torch.from_numpy(d["s0"].copy())
+    if via_bench:
+        # the benchmark's sharded leg: its rank logic times whole walks and single merges, max over ranks
+        import time
+        import bench
+
+        def timer(fn):
+            t = time.perf_counter()
+            fn()
+            return time.perf_counter() - t
+        probe = torch.zeros((B,), dtype=torch.int64)
+        m = bench.sharded_measure(lambda: walk.walk(s0, G)[0], lambda: S.allreduce_max()(probe), 2, 1, world,
+                                  timer)
+        dist.destroy_process_group()
+        q.put((rank, m["tokens"].numpy(), (m["walk_s"], m["merge_s"]), (lo, hi)))
+        return
+    toks, states = walk.walk(s0, G)
     dist.destroy_process_group()
     q.put((rank, toks.numpy(), states.numpy(), (lo, hi)))
 
@@ -100,6 +116,34 @@ def test_sharded_walk_on_gloo_ranks_is_the_unsharded_walk(world, kind, T):
     for r in range(world):
         np.testing.assert_array_equal(res[r][0], ref["tokens"])
         np.testing.assert_allclose(res[r][1], ref["state"], rtol=0, atol=1e-6)
+
+
+def test_benchmark_sharded_leg_rank_logic_on_gloo_ranks():
+    """bench.py --sharded's rank logic (warm-up, barrier, timed walks and merges, max over ranks) drives the
+    protocol on two gloo ranks: every rank gets the unsharded oracle's tokens and the same (slowest rank's)
+    times."""
+    from oracle import oracle as O
+    import whead_inputs as I
+    world = 2
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, world, port, MARKOV, 1.0, q, True)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = {}
+    for _ in procs:
+        rank, toks, times, bounds = q.get(timeout=300)
+        res[rank] = (toks, times)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    d = I.make_inputs(MARKOV, 333, 32, 2, 5, seed=4)
+    ref = O.walk(MARKOV, d["W"], d["E"], d["base"], d["s0"], T=1.0, seed=17)
+    for r in range(world):
+        np.testing.assert_array_equal(res[r][0], ref["tokens"])
+        assert res[r][1][0] > 0 and res[r][1][1] > 0
+    assert res[0][1] == res[1][1]
 
 
 def test_shard_bounds_cover_the_vocabulary_on_group_boundaries():

@@ -6,7 +6,8 @@ scratch is one fixed device array inside the library, shared by every call. This
 the C ABI twice in a row for each case (so the second call runs on the array the first call left behind)
 and compares tokens and fp32 logits with whead_walk on the same inputs, under the parity tolerance used by
 the other GPU tests (tokens identical; logits within 2e-2 times the logit RMS; here they are identical,
-since both run the same kernel). It lives in its own file so that pytest collects it last.
+since both run the same kernel). Around the second call it also checks that the device's free memory does
+not change. It lives in its own file so that pytest collects it last.
 """
 import numpy as np
 import pytest
@@ -59,9 +60,16 @@ def test_noalloc_matches_regular_entry_point_twice(torch_cuda, kind, V, r, B, ga
         tok = torch.full((B, gamma), -1, dtype=torch.int32, device=dev)
         z = torch.full((B, gamma, V), float("nan"), dtype=torch.float32, device=dev)
         status = torch.full((1,), 12345, dtype=torch.int32, device=dev)
+        torch.cuda.synchronize()
+        # the first call on a device may load the library's device code (and with it the scratch array); the
+        # second call must leave the device's free memory and torch's allocations exactly as they were
+        free0, held0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
         wh.walk_noalloc(W, E, base, s0, kind=kind, A=A, c=c, T=T, seed=99, flags=wh.FLAG_LOGITS_F32,
                         out_tokens=tok, out_logits=z, out_status=status)
         torch.cuda.synchronize()
+        if call == 1:
+            assert torch.cuda.mem_get_info()[0] == free0, "the call changed the device's free memory"
+            assert torch.cuda.memory_allocated() == held0
         assert int(status.item()) == 0, f"call {call}: device status {int(status.item())}"
         np.testing.assert_array_equal(tok.cpu().numpy(), ref_tok, err_msg=f"call {call}")
         assert np.max(np.abs(z.cpu().numpy() - ref_z)) <= LOGIT_TOL * scale, f"call {call}"
