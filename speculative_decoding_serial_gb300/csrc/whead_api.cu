@@ -129,7 +129,9 @@ Plan make_plan(int64_t V, int r, int kind, int Bcap, int NH, int sm_count, int s
     const int rf_per_q = (n_rf + 3) / 4;
     const int tmem_warps_per_q = (kWarps / 4) - rf_per_q;
     if (n_tmem > 0 && tmem_warps_per_q < 1) return false;
-    // relative cost of a group by tier, measured on GB300: tensor memory 5, register 5, shared 6, streamed 9
+    // relative cost of a group by tier, measured on GB300: tensor memory 5, register 5, shared 6, streamed 9. A
+    // register warp runs its shared-memory groups slower (its resident group leaves fewer registers for loads in
+    // flight): 8 there.
     int load[kWarps] = {};
     int sp_load[4] = {};
     auto push = [&](int w, uint32_t entry, int cost) -> bool {
@@ -150,24 +152,27 @@ Plan make_plan(int64_t V, int r, int kind, int Bcap, int NH, int sm_count, int s
       const int w = q + 4 * (idx % tmem_warps_per_q);
       if (!push(w, wl_entry(n_smem + i, kTierTmem, idx * 16 * KB), 5)) return false;
     }
-    // least-loaded sub-partition, then its least-loaded eligible warp
-    auto place = [&](uint32_t entry, int cost, bool rf_ok) -> bool {
+    // least-loaded sub-partition, then its warp with the least load after the group (cost_rf on register warps)
+    auto place = [&](uint32_t entry, int cost, bool rf_ok, int cost_rf) -> bool {
+      auto cost_on = [&](int w) { return ((out.rf_warp_mask >> w) & 1u) ? cost_rf : cost; };
       int bq = -1, bw = -1;
       for (int q = 0; q < 4; ++q) {
         int w_best = -1;
         for (int w = q; w < kWarps; w += 4)
-          if ((rf_ok || !((out.rf_warp_mask >> w) & 1u)) && (w_best < 0 || load[w] < load[w_best])) w_best = w;
+          if ((rf_ok || !((out.rf_warp_mask >> w) & 1u)) &&
+              (w_best < 0 || load[w] + cost_on(w) < load[w_best] + cost_on(w_best)))
+            w_best = w;
         if (w_best >= 0 && (bq < 0 || sp_load[q] < sp_load[bq])) {
           bq = q;
           bw = w_best;
         }
       }
-      return bw >= 0 && push(bw, entry, cost);
+      return bw >= 0 && push(bw, entry, cost_on(bw));
     };
     for (int i = 0; i < n_stream; ++i)
-      if (!place(wl_entry(n_smem + n_tmem + n_rf + i, kTierStream, 0), 9, true)) return false;
+      if (!place(wl_entry(n_smem + n_tmem + n_rf + i, kTierStream, 0), 9, true, 9)) return false;
     for (int j = 0; j < n_smem; ++j)
-      if (!place(wl_entry(j, kTierSmem, 0), 6, true)) return false;
+      if (!place(wl_entry(j, kTierSmem, 0), 6, true, 8)) return false;
     // recurrent: the slice of A h goes to the least-loaded warp that keeps no register group (the register warps'
     // copy of the step loop does not carry that code)
     if (recurrent) {
