@@ -9,8 +9,10 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libwhead.so")
-# the host library and the two halves of the walk kernel's instantiations, compiled in parallel
-SOURCES = [os.path.join(CSRC, n) for n in ("whead_api.cu", "walk_resident.cu", "walk_async.cu")]
+# the host library and the walk kernel's instantiations (Markov / recurrent head x base logits read at each step /
+# copied a step ahead), compiled in parallel
+SOURCES = [os.path.join(CSRC, n) for n in ("whead_api.cu", "walk_resident.cu", "walk_resident_rec.cu",
+                                           "walk_async.cu", "walk_async_rec.cu")]
 DEPS = SOURCES + [os.path.join(CSRC, n) for n in ("walk_kernel.cuh", "walk_launch.cuh", "walk_launch.h")] + [
     os.path.join(ROOT, "include", "whead.h")]
 # measurement-only library used by the benchmark for the roofline's on-chip figures

@@ -735,8 +735,9 @@ __device__ __forceinline__ unsigned long long read_walk_slots(const unsigned lon
 // own the tensor-memory groups of their lane quadrant (plus shared-memory groups). The two roles run
 // separately compiled copies of the step loop so that neither pays for the other's registers.
 // F8: E4M3 weights. ASYNC: each step's base logits are copied asynchronously a step ahead into a second
-// buffer (walks that read them from host memory); kept out of the other variants' step loop.
-template <int KB, int NH, bool NB1, bool F8, bool ASYNC>
+// buffer (walks that read them from host memory); kept out of the other variants' step loop. REC: the recurrent
+// head (the Markov head's copy carries none of its code: no A h slices, no tanh advance).
+template <int KB, int NH, bool NB1, bool F8, bool ASYNC, bool REC>
 __global__ void __launch_bounds__(kThreads, 1)
     walk_kernel(const __grid_constant__ CUtensorMap tmapW, const __grid_constant__ CUtensorMap tmapW128,
                 const __grid_constant__ WalkArgs P) {
@@ -746,7 +747,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int G = gridDim.x, cta = blockIdx.x;
   const int r = P.r, B = P.B, gamma = P.gamma;
   const int64_t V = P.V;
-  const bool recurrent = P.kind == 1;
+  constexpr bool recurrent = REC;  // the host launches the instantiation of the head's kind
 
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);

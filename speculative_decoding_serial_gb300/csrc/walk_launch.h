@@ -27,8 +27,11 @@ struct WalkLaunch {
 };
 
 // Cooperative launch of the walk kernel; WHEAD_OK, WHEAD_ERR_NO_COOP (grid not co-resident),
-// WHEAD_ERR_UNSUPPORTED (no instantiation for r / f8) or WHEAD_ERR_CUDA.
-int launch_walk_resident(const WalkLaunch& l, const WalkArgs& a);  // base logits read at each step
-int launch_walk_async(const WalkLaunch& l, const WalkArgs& a);     // base logits copied a step ahead
+// WHEAD_ERR_UNSUPPORTED (no instantiation for r / f8) or WHEAD_ERR_CUDA. The Markov and recurrent heads have
+// instantiations of their own, in translation units of their own (compiled in parallel).
+int launch_walk_resident_markov(const WalkLaunch& l, const WalkArgs& a);     // base logits read at each step
+int launch_walk_resident_recurrent(const WalkLaunch& l, const WalkArgs& a);
+int launch_walk_async_markov(const WalkLaunch& l, const WalkArgs& a);        // base logits copied a step ahead
+int launch_walk_async_recurrent(const WalkLaunch& l, const WalkArgs& a);
 
 }  // namespace whead

@@ -1,6 +1,6 @@
-// walk_resident.cu — walk kernel instantiations for base logits read at each step (device memory).
+// walk_resident.cu — walk kernel instantiations of the Markov head for base logits read at each step.
 #include "walk_launch.cuh"
 
 namespace whead {
-int launch_walk_resident(const WalkLaunch& l, const WalkArgs& a) { return launch_dispatch<false>(l, a); }
+int launch_walk_resident_markov(const WalkLaunch& l, const WalkArgs& a) { return launch_dispatch<false, false>(l, a); }
 }  // namespace whead

@@ -220,7 +220,9 @@ PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
 
 int launch(whead_t* h, const Plan& pl, const WalkArgs& a, int NH) {
   const WalkLaunch l{&h->tmap, &h->tmap128, h->stream, h->smem_optin, pl.G, pl.smem_bytes, h->p.r, NH, h->f8};
-  return (a.flags & kFlagBaseAsync) ? launch_walk_async(l, a) : launch_walk_resident(l, a);
+  if (a.kind == WHEAD_RECURRENT)
+    return (a.flags & kFlagBaseAsync) ? launch_walk_async_recurrent(l, a) : launch_walk_resident_recurrent(l, a);
+  return (a.flags & kFlagBaseAsync) ? launch_walk_async_markov(l, a) : launch_walk_resident_markov(l, a);
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -760,7 +762,7 @@ int noalloc_setup(int dev, NaDevice** out) {
 int noalloc_launch(int r, int NH, const CUtensorMap& tmap, const CUtensorMap& tmap128, cudaStream_t stream,
                    int smem_optin, const Plan& pl, const WalkArgs& a) {
   const WalkLaunch l{&tmap, &tmap128, stream, smem_optin, pl.G, pl.smem_bytes, r, NH, false};
-  return launch_walk_resident(l, a);
+  return a.kind == WHEAD_RECURRENT ? launch_walk_resident_recurrent(l, a) : launch_walk_resident_markov(l, a);
 }
 
 }  // namespace
