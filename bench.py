@@ -542,6 +542,13 @@ def ours(args, world, rank, local):
         slope = sum((a - gm) * (b - tm) for a, b in zip(fit_g, fit_t)) / sum((a - gm) ** 2 for a in fit_g)
         intercept = tm - slope * gm
 
+    phases = trace_phases(torch, head, base, s0, tok, w, plan, flush, stream, dev)
+    clocks["kernel_sm_mhz"] = phases.pop("kernel_sm_mhz")
+    clocks["kernel_sm_mhz_source"] = ("clock64 / globaltimer stamps of every CTA over the traced walks run right "
+                                      "after the timed region (the timed region is shorter than one nvidia-smi "
+                                      "sample)")
+    traffic = recorded_traffic() if args.workload == DEFAULT_WORKLOAD else None
+
     # roofline (on-chip operand bandwidth for the steps, HBM for the one-time shard load)
     hbm_gbs, peak_kind = load_peaks()
     onchip = probe_onchip()
@@ -553,7 +560,12 @@ def ours(args, world, rank, local):
     smem_min = max(0, w_per_sm - TMEM_BYTES - RF_W_BYTES_CAP)
     tmem_used = min(TMEM_BYTES, w_per_sm)
     t_star_clk = max(smem_min / smem_bpc, tmem_used / tmem_bpc)
-    mhz = clocks["sm_mhz"] or 1447.0
+    # the same bound for the placement the library actually ships for this walk (its shared and tensor-memory groups)
+    group_bytes = 16 * r * 2
+    t_star_shipped_clk = max(plan["smem_groups"] * group_bytes / smem_bpc, plan["tmem_groups"] * group_bytes / tmem_bpc)
+    # cycles to time at the clock the kernel ran at (its own stamps), else the sampled one
+    mhz = clocks["kernel_sm_mhz"] or clocks["sm_mhz"] or 1447.0
+    clock_source = "kernel stamps" if clocks["kernel_sm_mhz"] else ("nvidia-smi" if clocks["sm_mhz"] else "fallback")
     t_star_us = t_star_clk / mhz
     t_entry_us = wbytes / (hbm_gbs * 1e3)
     t_roof_us = t_entry_us + gamma * t_star_us
@@ -561,12 +573,6 @@ def ours(args, world, rank, local):
     achieved = alg_bytes / (us_per_walk * 1e3)
     peak = alg_bytes / (t_roof_us * 1e3)
 
-    phases = trace_phases(torch, head, base, s0, tok, w, plan, flush, stream, dev)
-    clocks["kernel_sm_mhz"] = phases.pop("kernel_sm_mhz")
-    clocks["kernel_sm_mhz_source"] = ("clock64 / globaltimer stamps of every CTA over the traced walks run right "
-                                      "after the timed region (the timed region is shorter than one nvidia-smi "
-                                      "sample)")
-    traffic = recorded_traffic() if args.workload == DEFAULT_WORKLOAD else None
 
     # end to end through the host-buffer entry point: pinned inputs copied in, tokens copied out
     base_h = torch.from_numpy(d["base"]).pin_memory()
@@ -604,10 +610,12 @@ def ours(args, world, rank, local):
                                         "committed profile taken on this kernel source (sha-matched)")
                      if traffic is not None else None,
                      "t_roof_us": t_roof_us, "t_entry_us": t_entry_us, "t_star_clk_per_step": t_star_clk,
-                     "hbm_peak_gbs": hbm_gbs, "hbm_peak_kind": peak_kind, "clock_mhz": mhz,
+                     "hbm_peak_gbs": hbm_gbs, "hbm_peak_kind": peak_kind, "clock_mhz": mhz, "clock_source": clock_source,
                      "onchip_measured": onchip,
                      "onchip_kind": "measured" if onchip else "fallback (128 B/clk shared, 428 B/clk tensor memory)"},
         "per_step": {"slope_us": slope, "intercept_us": intercept, "gammas": fit_g, "median_us": fit_t,
+                     "t_star_shipped_placement_clk": t_star_shipped_clk,
+                     "frac_of_shipped_placement_bound": (t_star_shipped_clk / mhz / slope) if slope else None,
                      "t_star_us": t_star_us,
                      "frac_of_onchip_roofline": (t_star_us / slope) if slope else None},
         "cpu_baseline": cpu,

@@ -9,6 +9,8 @@ the other GPU tests (tokens identical; logits within 2e-2 times the logit RMS; h
 since both run the same kernel). Around the second call it also checks that the device's free memory does
 not change. It lives in its own file so that pytest collects it last.
 """
+import gc
+
 import numpy as np
 import pytest
 
@@ -62,14 +64,21 @@ def test_noalloc_matches_regular_entry_point_twice(torch_cuda, kind, V, r, B, ga
         status = torch.full((1,), 12345, dtype=torch.int32, device=dev)
         torch.cuda.synchronize()
         # the first call on a device may load the library's device code (and with it the scratch array); the
-        # second call must leave the device's free memory and torch's allocations exactly as they were
-        free0, held0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
-        wh.walk_noalloc(W, E, base, s0, kind=kind, A=A, c=c, T=T, seed=99, flags=wh.FLAG_LOGITS_F32,
-                        out_tokens=tok, out_logits=z, out_status=status)
-        torch.cuda.synchronize()
+        # second call must leave the device's free memory and torch's allocations exactly as they were (the
+        # garbage collector is held off meanwhile, so that no unrelated tensor is freed during the call)
+        gc.collect()
+        gc.disable()
+        try:
+            free0, held0 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+            wh.walk_noalloc(W, E, base, s0, kind=kind, A=A, c=c, T=T, seed=99, flags=wh.FLAG_LOGITS_F32,
+                            out_tokens=tok, out_logits=z, out_status=status)
+            torch.cuda.synchronize()
+            free1, held1 = torch.cuda.mem_get_info()[0], torch.cuda.memory_allocated()
+        finally:
+            gc.enable()
         if call == 1:
-            assert torch.cuda.mem_get_info()[0] == free0, "the call changed the device's free memory"
-            assert torch.cuda.memory_allocated() == held0
+            assert free1 == free0, "the call changed the device's free memory"
+            assert held1 == held0, "the call allocated through torch"
         assert int(status.item()) == 0, f"call {call}: device status {int(status.item())}"
         np.testing.assert_array_equal(tok.cpu().numpy(), ref_tok, err_msg=f"call {call}")
         assert np.max(np.abs(z.cpu().numpy() - ref_z)) <= LOGIT_TOL * scale, f"call {call}"
