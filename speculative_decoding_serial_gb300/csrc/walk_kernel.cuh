@@ -950,6 +950,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t box_stride = (uint32_t)(P.n_smem * kBoxBytes);
   const float T = P.T;
   const bool sampled = T > 0.0f;
+  const bool t_is_one = T == 1.0f;  // z / 1 is z exactly: the correctly rounded division is skipped
   const bool want_f32 = (P.flags & kFlagLogitsF32) != 0u;
 
   // ---------------- the walk ----------------
@@ -1197,7 +1198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   if (want_f32) reinterpret_cast<float*>(P.logits)[obase + lr + u] = zz[u];
                   else reinterpret_cast<__nv_bfloat16*>(P.logits)[obase + lr + u] = __float2bfloat16_rn(zz[u]);
                 }
-                const float key = __fadd_rn(__fdiv_rn(zz[u], T), gumbel_from_word(ww[u]));
+                const float key = __fadd_rn(t_is_one ? zz[u] : __fdiv_rn(zz[u], T), gumbel_from_word(ww[u]));
                 bestk = umax64(bestk, pack_key(key, v0 + (uint32_t)u));
               }
             }
@@ -1240,7 +1241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (want_f32) reinterpret_cast<float*>(P.logits)[obase + lr + u] = zz[u];
                     else reinterpret_cast<__nv_bfloat16*>(P.logits)[obase + lr + u] = __float2bfloat16_rn(zz[u]);
                   }
-                  const float key = __fadd_rn(__fdiv_rn(zz[u], T), gumbel_from_word(ww[u]));
+                  const float key = __fadd_rn(t_is_one ? zz[u] : __fdiv_rn(zz[u], T), gumbel_from_word(ww[u]));
                   bestk = umax64(bestk, pack_key(key, v0 + (uint32_t)u));
                 }
               }
