@@ -97,3 +97,30 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(torch_cuda):
     with pytest.raises(wh.WheadError) as e:
         wh.walk_noalloc(W, E, base, s0, out_tokens=tok)
     assert e.value.code == wh.ERR_UNSUPPORTED
+
+
+def test_noalloc_reports_a_timeout_and_the_next_call_is_correct(torch_cuda):
+    """A walk whose bounded waits run out (CTA 0 skips its first arrival: a host flag, no fault) reports
+    WHEAD_ERR_TIMEOUT through the caller's status word (and check=True raises it); the next call on the same shared
+    scratch array, which the call clears first, gives the regular entry point's tokens again."""
+    torch = torch_cuda
+    from speculative_decoding_serial_gb300 import whead as wh
+
+    d = I.make_inputs(0, 40000, 128, 2, 3, seed=2)
+    W = torch.from_numpy(d["W"].view(np.int16)).view(torch.bfloat16).cuda()
+    E = torch.from_numpy(d["E"].view(np.int16)).view(torch.bfloat16).cuda()
+    base = torch.from_numpy(d["base"]).cuda()
+    s0 = torch.from_numpy(d["s0"]).cuda()
+    tok = torch.empty((2, 3), dtype=torch.int32, device="cuda")
+    status = torch.zeros((1,), dtype=torch.int32, device="cuda")
+    with pytest.raises(wh.WheadError) as e:
+        wh.walk_noalloc(W, E, base, s0, flags=wh.FLAG_FAULT_SKIP_ARRIVAL, timeout_us=20000, out_tokens=tok,
+                        out_status=status, check=True)
+    assert e.value.code == wh.ERR_TIMEOUT
+    assert int(status.item()) == wh.ERR_TIMEOUT
+    head = wh.Head(W, E, kind=0, max_B=2, max_gamma=3)
+    ref = head.walk(base, s0).cpu().numpy()
+    assert head.status() == 0
+    head.close()
+    wh.walk_noalloc(W, E, base, s0, out_tokens=tok, out_status=status, check=True)
+    np.testing.assert_array_equal(tok.cpu().numpy(), ref)
