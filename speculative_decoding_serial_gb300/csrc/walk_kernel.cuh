@@ -50,6 +50,8 @@ constexpr int kMaxGrid = 256;  // CTAs per walk: the exchange reads up to 8 slot
 constexpr int kGroupRows = 16;
 constexpr int kBoxBytes = kGroupRows * 128;  // one 16-row x 64-element bf16 box
 constexpr int kTmaChunkGroups = 8;           // groups per large TMA copy (128 rows x 64 elements)
+constexpr int kMaxStaged = 64;  // staged groups of the ring entry (their barriers sit in the exchange words)
+static_assert(kMaxStaged * 12 <= kWarps * kMaxB * 8, "the ring's barriers and flags fit in the exchange words");
 
 // device status codes (match the public WHEAD_ERR_* values)
 constexpr int kStatusTimeout = -4;
@@ -780,10 +782,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t my_entry = (lane < my_count) ? P.wl[warp][lane] : 0u;
   const bool rf_warp = (P.rf_warp_mask >> warp) & 1u;
 
+  // Shard load through a ring (r = 256, bf16 weights): the shared tier's n_smem slots first receive the
+  // tensor-memory and register groups, which their owner warps move on, and then their own groups, so that the
+  // whole shard streams in by TMA with every slot's copy in flight. Staged group k (local group n_smem + k)
+  // passes through slot k % n_smem and completes on barrier k, used for one phase only. The barriers and the
+  // issue flags sit in the exchange words, which the walk uses only after the entry.
+  constexpr bool kRingEntry = KB == 4 && !F8;
+  const int n_st = P.n_tmem + P.n_rf;  // staged groups
+  const bool ring = kRingEntry && P.n_smem > 0 && n_st > 0 && n_st <= kMaxStaged;
+  volatile int* s_issued = reinterpret_cast<volatile int*>(s_red + kMaxStaged);  // [n_st] staged copy issued
+  auto stage_bar = [&](int k) { return smem_u32(s_red + k); };
+
   // ---------------- set-up ----------------
   if (tid == 0) {
     *s_abort = 0;
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(mbar) : "memory");
+    if (ring)
+      for (int k = 0; k < n_st; ++k) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"(stage_bar(k)) : "memory");
+        s_issued[k] = 0;
+      }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
   }
@@ -807,7 +825,35 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t lane_quadrant = (uint32_t)(32 * (warp & 3)) << 16;
 
   // ---------------- entry: load the shard once (Fig. 4: the one-time shard load) ----------------
-  if (tid == 0 && P.n_smem > 0) {
+  // one group (16 rows, KB boxes) into slot s of the shared tier, completing on barrier bar
+  auto issue_group = [&](int s, int j, uint32_t bar) {
+    const int y = (int)(row_base + (int64_t)kGroupRows * j);
+#pragma unroll
+    for (int bx = 0; bx < KB; ++bx)
+      asm volatile(
+          "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+              smem_u32(sW) + (uint32_t)(bx * P.n_smem + s) * kBoxBytes),
+          "l"(reinterpret_cast<uint64_t>(&tmapW)), "r"(64 * bx), "r"(y), "r"(bar)
+          : "memory");
+  };
+  // the next copy into slot s once staged group k has left it: staged group k + n_smem, else the slot's own group
+  auto refill = [&](int s, int k) {
+    const int k2 = k + P.n_smem;
+    if (k2 < n_st) {
+      s_issued[k2] = 1;
+      asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(stage_bar(k2)), "r"(KB * kBoxBytes)
+                   : "memory");
+      issue_group(s, P.n_smem + k2, stage_bar(k2));
+    } else {
+      issue_group(s, s, mbar);
+    }
+  };
+  if (tid == 0 && ring) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(mbar), "r"(P.n_smem * KB * kBoxBytes)
+                 : "memory");
+    for (int s = 0; s < P.n_smem; ++s) refill(s, s - P.n_smem);
+  }
+  if (tid == 0 && P.n_smem > 0 && !ring) {
     // box-major shared tier: box bx of local group j at (bx * n_smem + j) * 2048. Runs of 8 groups go in one
     // 128-row copy, the remainder in 16-row copies.
     const uint32_t bytes = (uint32_t)(P.n_smem * KB * kBoxBytes);
@@ -835,11 +881,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   }
-  stage_base(P, s_base, row_base, 0, 0, kThreads);
-  if constexpr (base_async) copy_base_async(P, s_base_in, row_base, 1, 32, kThreads - 32);
+  if (!ring) {
+    stage_base(P, s_base, row_base, 0, 0, kThreads);
+    if constexpr (base_async) copy_base_async(P, s_base_in, row_base, 1, 32, kThreads - 32);
+  }
 
-  // tensor-memory groups of this warp: global -> registers (all boxes of a group in flight) -> tcgen05.st
-  if (!rf_warp) {
+  // without the ring (r below 256, E4M3 weights): the tensor-memory groups of this warp go global -> registers
+  // (all boxes of a group in flight) -> tcgen05.st
+  if (!rf_warp && !ring) {
     for (int e = 0; e < my_count; ++e) {
       const uint32_t ent = __shfl_sync(0xffffffffu, my_entry, e);
       if (((ent >> 8) & 3u) != kTierTmem) continue;
@@ -858,15 +907,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-  // register-resident group of a register warp: its loads are issued here, so they land while the rest of the
-  // entry runs (register warps own no tensor-memory group)
+  // register-resident group of a register warp (register warps own no tensor-memory group): without the ring its
+  // loads are issued here, so they land while the rest of the entry runs; with it, the group comes through a slot
   uint32_t rfA[KB][16];
   if (NH == 1 && rf_warp) {  // the planner gives register groups only to batches of up to 8 walks
     int jr = -1;
-    for (int e = 0; e < my_count; ++e) {
-      const uint32_t ent = __shfl_sync(0xffffffffu, my_entry, e);
-      if (((ent >> 8) & 3u) == kTierRf) jr = (int)(ent & 0xFFu);
-    }
+    if (!ring)
+      for (int e = 0; e < my_count; ++e) {
+        const uint32_t ent = __shfl_sync(0xffffffffu, my_entry, e);
+        if (((ent >> 8) & 3u) == kTierRf) jr = (int)(ent & 0xFFu);
+      }
 #pragma unroll
     for (int bx = 0; bx < KB; ++bx) {
       if (jr >= 0) {
@@ -878,6 +928,50 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < 16; ++i) rfA[bx][i] = 0u;
       }
     }
+  }
+  // ring: each warp takes its staged groups out of their slots in the order they were issued (staged group k
+  // sits in slot k % n_smem in round k / n_smem), then hands the slot on
+  if (ring) {
+    const uint32_t off0 = (uint32_t)(((2 * c) ^ g) << 4), off1 = (uint32_t)(((2 * c + 1) ^ g) << 4);
+    for (int e = 0; e < my_count; ++e) {
+      const uint32_t ent = __shfl_sync(0xffffffffu, my_entry, e);
+      const uint32_t tier = (ent >> 8) & 3u;
+      if (tier != kTierTmem && tier != kTierRf) continue;
+      const int k = (int)(ent & 0xFFu) - P.n_smem, sl = k % P.n_smem;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(stage_bar(k), 0u, P.timeout_ns))) {
+        if (lane == 0) atomicCAS(P.status, 0, kStatusTimeout);
+        *s_abort = 1;
+        break;
+      }
+      const uint32_t taddr = tmem_base + lane_quadrant + (ent >> 16);
+#pragma unroll
+      for (int bx = 0; bx < KB; ++bx) {
+        // the 128-byte-swizzled box: row g's chunks 2c and 2c + 1 and the same chunks of row g + 8
+        const uint8_t* box = sW + (uint32_t)(bx * P.n_smem + sl) * kBoxBytes;
+        const uint4 r0 = *reinterpret_cast<const uint4*>(box + g * 128 + off0);
+        const uint4 s0 = *reinterpret_cast<const uint4*>(box + (g + 8) * 128 + off0);
+        const uint4 r1 = *reinterpret_cast<const uint4*>(box + g * 128 + off1);
+        const uint4 s1 = *reinterpret_cast<const uint4*>(box + (g + 8) * 128 + off1);
+        const uint32_t a[16] = {r0.x, r0.y, r0.z, r0.w, s0.x, s0.y, s0.z, s0.w,
+                                r1.x, r1.y, r1.z, r1.w, s1.x, s1.y, s1.z, s1.w};
+        if (tier == kTierTmem) {
+          uint32_t q[16];
+          rows_to_fragments(q, a);
+          tmem_st16(taddr + 16 * bx, q);
+        } else if (NH == 1) {
+          rows_to_fragments(rfA[bx], a);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        refill(sl, k);
+      }
+      __syncwarp();
+    }
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+    stage_base(P, s_base, row_base, 0, 0, kThreads);
+    if constexpr (base_async) copy_base_async(P, s_base_in, row_base, 1, 32, kThreads - 32);
   }
   // streamed groups: ask L2 for their rows now, so that every step reads them from L2
   for (int e = 0; e < my_count; ++e) {
@@ -907,7 +1001,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // wait for the TMA copies (bounded)
   bool tma_done = true;
   if (P.n_smem > 0) {
-    tma_done = mbar_wait_bounded(mbar, 0u, P.timeout_ns);
+    tma_done = __all_sync(0xffffffffu, mbar_wait_bounded(mbar, 0u, P.timeout_ns));
     if (!tma_done) {
       if (tid == 0) atomicCAS(P.status, 0, kStatusTimeout);
       *s_abort = 1;
@@ -944,6 +1038,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   tmem_fence_before();
   __syncthreads();
   tmem_fence_after();
+  // the slot barriers' words become exchange words again (first written after the first step's projection and
+  // barrier)
+  if (ring) {
+    if (!*s_abort) {
+      if (tid < n_st) asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(stage_bar(tid)) : "memory");
+    } else if (tid == 0) {
+      // a wait of the entry timed out: copies still in flight land before the walk is skipped and the CTA exits
+      for (int k = 0; k < n_st; ++k)
+        if (s_issued[k]) (void)mbar_wait_bounded(stage_bar(k), 0u, P.timeout_ns);
+    }
+  }
   trace_stamp(P, 1);
 
   const uint8_t* sW_c = sW;
