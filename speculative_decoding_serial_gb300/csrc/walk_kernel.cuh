@@ -782,14 +782,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t my_entry = (lane < my_count) ? P.wl[warp][lane] : 0u;
   const bool rf_warp = (P.rf_warp_mask >> warp) & 1u;
 
-  // Shard load through a ring (r = 256, bf16 weights): the shared tier's n_smem slots first receive the
-  // tensor-memory and register groups, which their owner warps move on, and then their own groups, so that the
-  // whole shard streams in by TMA with every slot's copy in flight. Staged group k (local group n_smem + k)
-  // passes through slot k % n_smem and completes on barrier k, used for one phase only. The barriers and the
-  // issue flags sit in the exchange words, which the walk uses only after the entry.
-  constexpr bool kRingEntry = KB == 4 && !F8;
+  // Shard load through a ring: the shared tier's n_smem slots first receive the tensor-memory and register
+  // groups, which their owner warps move on, and then their own groups, so that the whole shard streams in by TMA
+  // with every slot's copy in flight. Staged group k (local group n_smem + k) passes through slot k % n_smem and
+  // completes on barrier k, used for one phase only. The barriers and the issue flags sit in the exchange words,
+  // which the walk uses only after the entry. Without a shared tier, or with more than kMaxStaged groups to
+  // stage, the tensor-memory and register groups are loaded through registers instead.
   const int n_st = P.n_tmem + P.n_rf;  // staged groups
-  const bool ring = kRingEntry && P.n_smem > 0 && n_st > 0 && n_st <= kMaxStaged;
+  const bool ring = P.n_smem > 0 && n_st > 0 && n_st <= kMaxStaged;
   volatile int* s_issued = reinterpret_cast<volatile int*>(s_red + kMaxStaged);  // [n_st] staged copy issued
   auto stage_bar = [&](int k) { return smem_u32(s_red + k); };
 
@@ -886,8 +886,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if constexpr (base_async) copy_base_async(P, s_base_in, row_base, 1, 32, kThreads - 32);
   }
 
-  // without the ring (r below 256, E4M3 weights): the tensor-memory groups of this warp go global -> registers
-  // (all boxes of a group in flight) -> tcgen05.st
+  // without the ring: the tensor-memory groups of this warp go global -> registers (all boxes of a group in
+  // flight) -> tcgen05.st
   if (!rf_warp && !ring) {
     for (int e = 0; e < my_count; ++e) {
       const uint32_t ent = __shfl_sync(0xffffffffu, my_entry, e);
