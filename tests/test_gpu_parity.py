@@ -400,6 +400,11 @@ CAPPED = [
     (3, (0, 0, 3)),
     (1, (13, 0, 0)),
     (1, (0, 0, 0)),
+    # the shard load's ring: twelve staged groups through one slot (register groups in the last rounds), eight
+    # through two slots with two batch halves, and as many staged groups as slots
+    (1, (1, 8, 4)),
+    (9, (2, 8, 0)),
+    (1, (4, 4, 0)),
 ]
 
 
