@@ -54,18 +54,21 @@ def recorded_traffic():
 
 
 def probe_onchip():
-    """Shared/tensor-memory bytes per SM clock, mma.sync and thin-N tcgen05.mma clocks per op, grid-exchange clocks."""
+    """Shared/tensor-memory bytes per SM clock, mma.sync and thin-N tcgen05.mma clocks per op, grid-exchange clocks,
+    and the clocks of tcgen05.mma and mma.sync run alone and side by side (do they share the tensor pipe)."""
     import ctypes
     from speculative_decoding_serial_gb300 import build
     try:
         L = ctypes.CDLL(build.PROBE_LIB)
-        out = (ctypes.c_double * 6)()
+        out = (ctypes.c_double * 9)()
         rc = L.whead_probe_onchip(out)
         if rc != 0:
             return None
         return {"smem_b_per_clk": out[0], "tmem_b_per_clk": out[1], "mma_m16n8k16_clk_per_sm": out[2],
                 "grid_exchange_clk": out[3], "tcgen05_m128n16k16_clk_1_issuer": out[4],
-                "tcgen05_m128n16k16_clk_4_issuers": out[5]}
+                "tcgen05_m128n16k16_clk_4_issuers": out[5],
+                "tcgen05_beside_mma_sync_clk": {"tcgen05_alone": out[6], "mma_sync_alone": out[7],
+                                                "mma_sync_with_tcgen05": out[8]}}
     except OSError:
         return None
 

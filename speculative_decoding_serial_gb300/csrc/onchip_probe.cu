@@ -10,8 +10,12 @@
 //     out[4] SM clocks per tcgen05.mma.cta_group::1.kind::f16 of shape M128 N16 K16 (A and B in shared memory,
 //            128-byte swizzle, D in tensor memory), one issuing thread
 //     out[5] the same with four issuing threads (one per warp, separate accumulators)
-// The last two say how fast the fifth-generation tensor core consumes a thin (N <= 16) operand: W bytes per
-// clock = 4096 / out[5], against 256 B per clock for mma.sync.m16n8k16 at out[2] = 2.
+//     out[6] SM clocks for 256 of those M128 N16 K16 instructions from one thread while 11 warps stay idle
+//     out[7] SM clocks for 11 warps running 800 mma.sync.m16n8k16 each while that thread stays idle
+//     out[8] SM clocks for the 11 warps' mma.sync when the thread issues its tcgen05.mma at the same time
+// out[4] and out[5] say how fast the fifth-generation tensor core consumes a thin (N <= 16) operand: W bytes per
+// clock = 4096 / out[5], against 256 B per clock for mma.sync.m16n8k16 at out[2] = 2. out[6..8] say whether the
+// two can share the projection: if they ran side by side, out[8] would stay near out[7].
 // Every wait is bounded; every access stays inside its buffer. Returns 0, or a negative CUDA error.
 #include <cuda_runtime.h>
 
@@ -233,6 +237,95 @@ __global__ void __launch_bounds__(128, 1) umma_rate(long long* cyc, int* status,
   if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(256) : "memory");
 }
 
+// tcgen05.mma beside mma.sync. mode 0: warp 11's lane 0 issues `tiles` x 16 M128 N16 K16 (A and B in shared
+// memory as above, one accumulator) and waits for them (bounded by 100 ms); mode 1: warps 0-10 run `iters` x 8
+// independent mma.sync; mode 2: both at once. cyc[2 b] = the tcgen05 issuer's clocks, cyc[2 b + 1] = the slowest
+// mma.sync warp's.
+__global__ void __launch_bounds__(kThreads, 1) umma_beside_mma(long long* cyc, int* status, float* sink, int mode,
+                                                               int tiles, int iters) {
+  extern __shared__ uint8_t umma_smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(umma_smem_raw) + 1023) & ~(uintptr_t)1023);
+  uint64_t* mbar = reinterpret_cast<uint64_t*>(sm + kUmmaABytes + kUmmaBBytes);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(mbar + 2);
+  __shared__ long long s_t[kThreads / 32];
+  const int tid = threadIdx.x, warp = tid / 32, lane = tid % 32;
+  for (int i = tid; i < (kUmmaABytes + kUmmaBBytes) / 16; i += blockDim.x) reinterpret_cast<uint4*>(sm)[i] = make_uint4(0, 0, 0, 0);
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"((uint32_t)__cvta_generic_to_shared(s_tmem)),
+                 "r"(32) : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  if (tid == 0) asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;" ::"r"((uint32_t)__cvta_generic_to_shared(mbar)) : "memory");
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+  const uint32_t tmem = *s_tmem;
+  const long long t0 = clock64();
+  long long t = 0;
+  if (warp == kThreads / 32 - 1) {
+    if (lane == 0 && mode != 1) {
+      const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | ((16u >> 3) << 17) | ((128u >> 4) << 24);
+      const uint32_t a0 = (uint32_t)__cvta_generic_to_shared(sm), b0 = a0 + kUmmaABytes;
+      const uint32_t mb = (uint32_t)__cvta_generic_to_shared(mbar);
+      for (int tile = 0; tile < tiles; ++tile) {
+#pragma unroll
+        for (int kk = 0; kk < 16; ++kk) {
+          const uint64_t ad = umma_sdesc(a0 + (uint32_t)((kk / 4) * 128 * 128 + (kk % 4) * 32));
+          const uint64_t bd = umma_sdesc(b0 + (uint32_t)((kk / 4) * 16 * 128 + (kk % 4) * 32));
+          asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+                       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n"
+                       ::"r"(tmem), "l"(ad), "l"(bd), "r"(idesc), "r"(kk > 0 ? 1u : 0u) : "memory");
+        }
+      }
+      asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mb) : "memory");
+      bool ok = false;
+      uint64_t ts, tn;
+      asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(ts));
+      tn = ts;
+      while (!ok && tn - ts < 100000000ull) {
+        uint32_t r;
+        asm volatile("{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], 0;\n selp.u32 %0, 1, 0, p;\n}\n"
+                     : "=r"(r) : "r"(mb) : "memory");
+        ok = r != 0;
+        asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(tn));
+      }
+      t = clock64() - t0;
+      if (!ok) atomicExch(status, 1);
+    }
+  } else if (mode != 0) {
+    const uint32_t a0 = tid, a1 = tid * 3u, a2 = tid * 5u, a3 = tid * 7u;
+    const uint32_t b0 = 0x3f803f80u, b1 = 0x3f803f80u;
+    float c[8][4];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.f;
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+            : "+f"(c[j][0]), "+f"(c[j][1]), "+f"(c[j][2]), "+f"(c[j][3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    }
+    float sum = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) sum += c[j][0] + c[j][1] + c[j][2] + c[j][3];
+    sink[blockIdx.x * blockDim.x + tid] = sum;
+    t = clock64() - t0;
+  }
+  if (lane == 0) s_t[warp] = t;
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+  __syncthreads();
+  if (tid == 0) {
+    long long mx = 0;
+    for (int w = 0; w < kThreads / 32 - 1; ++w) mx = s_t[w] > mx ? s_t[w] : mx;
+    cyc[2 * blockIdx.x] = s_t[kThreads / 32 - 1];
+    cyc[2 * blockIdx.x + 1] = mx;
+  }
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(32) : "memory");
+}
+
 double median_cycles(const long long* d_cyc, int n) {
   std::vector<long long> h(n);
   if (cudaMemcpy(h.data(), d_cyc, n * sizeof(long long), cudaMemcpyDeviceToHost) != cudaSuccess) return -1.0;
@@ -254,7 +347,7 @@ extern "C" int whead_probe_onchip(double* out) {
   const int smem_bytes = 192 * 1024;
   do {
     if (cudaMalloc(&d_out, (size_t)nsm * kThreads * 4) != cudaSuccess) { rc = -2; break; }
-    if (cudaMalloc(&d_cyc, (size_t)nsm * 8) != cudaSuccess) { rc = -2; break; }
+    if (cudaMalloc(&d_cyc, (size_t)nsm * 2 * 8) != cudaSuccess) { rc = -2; break; }
     if (cudaMalloc(&d_cnt, 256) != cudaSuccess) { rc = -2; break; }
     if (cudaMalloc(&d_status, 4) != cudaSuccess) { rc = -2; break; }
     if (cudaFuncSetAttribute(smem_bw, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) != cudaSuccess) { rc = -3; break; }
@@ -297,6 +390,26 @@ extern "C" int whead_probe_onchip(double* out) {
     out[5] = median_cycles(d_cyc, nsm) / 128.0;
     cudaMemcpy(&st, d_status, 4, cudaMemcpyDeviceToHost);
     if (st) out[4] = out[5] = -1.0;
+    // tcgen05.mma beside mma.sync: (tcgen05 alone, mma.sync alone, mma.sync with tcgen05 at the same time)
+    if (cudaFuncSetAttribute(umma_beside_mma, cudaFuncAttributeMaxDynamicSharedMemorySize, umma_smem) != cudaSuccess) { rc = -3; break; }
+    if (cudaMemset(d_status, 0, 4) != cudaSuccess) { rc = -4; break; }
+    float* d_sink = reinterpret_cast<float*>(d_out);  // nsm x kThreads floats
+    double med[3] = {0, 0, 0};
+    for (int mode = 0; mode < 3; ++mode) {
+      umma_beside_mma<<<nsm, kThreads, umma_smem>>>(d_cyc, d_status, d_sink, mode, 16, 100);  // warm-up
+      umma_beside_mma<<<nsm, kThreads, umma_smem>>>(d_cyc, d_status, d_sink, mode, 16, 100);
+      if (cudaDeviceSynchronize() != cudaSuccess) { rc = -4; break; }
+      std::vector<long long> h(2 * nsm), a(nsm);
+      if (cudaMemcpy(h.data(), d_cyc, 2 * nsm * sizeof(long long), cudaMemcpyDeviceToHost) != cudaSuccess) { rc = -4; break; }
+      for (int i = 0; i < nsm; ++i) a[i] = h[2 * i + (mode == 0 ? 0 : 1)];
+      std::sort(a.begin(), a.end());
+      med[mode] = (double)a[nsm / 2];
+    }
+    if (rc != 0) break;
+    cudaMemcpy(&st, d_status, 4, cudaMemcpyDeviceToHost);
+    out[6] = st ? -1.0 : med[0];
+    out[7] = med[1];
+    out[8] = st ? -1.0 : med[2];
   } while (false);
   if (d_out) cudaFree(d_out);
   if (d_cyc) cudaFree(d_cyc);
