@@ -1575,6 +1575,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = tid; i < B * r; i += kThreads) {
           const int n = i / r, k = i % r;
           const float e = __uint_as_float((uint32_t)P.E[(int64_t)s_win[n] * r + k] << 16);
+          const float ck = P.c ? P.c[k] : 0.f;  // loaded beside E's row, ahead of the slice reads
           unsigned long long word = 0ull;
           for (uint32_t spins = 0;; ++spins) {
             asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(word) : "l"(ah + i) : "memory");
@@ -1586,7 +1587,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (ah_late) break;
           float pre = __fadd_rn(__uint_as_float((uint32_t)word), e);
-          if (P.c) pre = __fadd_rn(pre, P.c[k]);
+          if (P.c) pre = __fadd_rn(pre, ck);
           s_h[i] = tanhf(pre);
         }
         if (ah_late) {
