@@ -1541,6 +1541,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
       // ---------------- state advance ----------------
       if (P.flags & kFlagFixedLatent) continue;
+      // after the last step the state is needed only when the caller asks for the states
+      if (t + 1 == gamma && P.state == nullptr) {
+        trace_stamp(P, 2 + kTraceStampsPerStep * t + 3);
+        break;
+      }
       if (!recurrent) {
         if constexpr (F8) {
           if constexpr (kParRead) {
