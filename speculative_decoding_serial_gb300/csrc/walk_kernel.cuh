@@ -11,8 +11,10 @@
 //
 // Design on GB300 (one persistent cooperative CTA of 384 threads per SM):
 //  - W is split into 16-row groups. Each CTA owns `ng` consecutive groups and keeps them in three
-//    on-chip tiers for the whole walk: shared memory (loaded once by TMA with the 128-byte swizzle),
-//    tensor memory (written once with tcgen05.st, read every step with tcgen05.ld) and registers.
+//    on-chip tiers for the whole walk: shared memory, tensor memory (written once with tcgen05.st, read
+//    every step with tcgen05.ld) and registers. The whole shard arrives by TMA (128-byte swizzle) through
+//    a ring of the shared-memory slots: they carry the tensor-memory and register groups first, which
+//    their warps move on, and then their own groups.
 //  - The projection of a group is 16 (r = 256) mma.sync.m16n8k16 bf16 -> fp32 ops whose A operand is
 //    the W group and whose B operand holds the bf16 states of up to 8 walks (two ops for 16 walks).
 //    The k index inside each 64-wide box is permuted so that one 16-byte shared-memory load gives a
