@@ -31,7 +31,7 @@ struct Plan {
 };
 
 struct Scratch {
-  unsigned long long* slots;  // [2 call parities][2 step parities][sm_count][kMaxB]
+  unsigned long long* slots;  // [2 call parities][2 step parities] x sm_count x kMaxB words (walk-major per call)
   unsigned int* cnt;          // two counters, 128 bytes apart
   unsigned long long* ah;     // [2 call parities][2 step parities][kMaxB][r] tagged words
   int* status;
@@ -718,7 +718,7 @@ int whead_destroy(whead_t* h) {
 // ------------------------------------------------------------------------------------------------
 namespace {
 
-// Layout of the array: [slots: 2 step parities x up to 256 CTAs x 16 walks, 64 KB][counter 128 B][status 128 B]
+// Layout of the array: [slots: 2 step parities x 16 walks x up to 256 CTAs, 64 KB][counter 128 B][status 128 B]
 // [tagged A h slices: 2 step parities x B x r words, up to 64 KB]. Slots, counter, status and the slices of
 // the call are cleared by the host before every call.
 constexpr int kNaMaxGrid = kMaxGrid;
