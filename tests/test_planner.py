@@ -48,6 +48,17 @@ def test_placements_of_the_pages_workloads(shape, want):
     assert p["threads"] == 384 and p["sm_count"] == 152
 
 
+@pytest.mark.parametrize("shape,want", MEASURED)
+def test_the_pages_workloads_load_through_the_ring(shape, want):
+    """The kernel streams the shard through its shared-memory slots when there is a shared tier and at most 64
+    tensor-memory and register groups to stage; every workload of the pages qualifies (the small head has nothing
+    to stage; a head that did not qualify would load those groups through registers instead)."""
+    V, r, kind, B, e4m3 = shape
+    p = wh.plan_query(V, r, kind, max_B=B, B=B, e4m3=e4m3, **GB300)
+    staged = p["tmem_groups"] + p["rf_groups"]
+    assert p["smem_groups"] >= 1 and staged <= 64
+
+
 def test_headline_placement_bytes():
     p = wh.plan_query(151936, 256, MARKOV, max_B=1, B=1, **GB300)
     assert p["smem_bytes"] == 227856 and p["tmem_cols"] == 512
@@ -93,6 +104,12 @@ def check_plan(p, V, r, kind, e4m3, sm_count, smem_optin):
         assert all(tiers[j] == tier for j in range(lo, hi))
     if kind == RECURRENT:
         assert not (rf_mask >> p["ah_warp"]) & 1
+    # the shard load's ring: every warp takes its staged (tensor-memory and register) groups out of the shared
+    # slots in work-list order, and the slot of staged group k is refilled only after group k - n_smem has left
+    # it, so each warp's staged groups must come in increasing order for the ring to always move on
+    for entries in p["work_lists"]:
+        staged = [j for j, tier, _ in entries if tier in (wh.TIER_TMEM, wh.TIER_RF)]
+        assert staged == sorted(staged)
 
 
 SHAPES = list(itertools.product(
